@@ -1,0 +1,417 @@
+// Split-KV paged decode for bf16 sink attention on sm_103a.
+//
+// One CTA owns (chunk c, KV head g, sequence b) and all G query heads of that
+// group, so every K/V byte of the chunk is read from HBM exactly once.
+// "GPT-OSS pada Hari ke-0", section "Atensi Sink": attention is parallelised
+// over heads and along the KV length; the online softmax starts its running
+// maximum at the head's sink value with running sum 1, and only the first
+// chunk of a split may do so.
+//
+// Warp roles (160 threads):
+//   warp 4      producer: reads the block table and issues one TMA box per
+//               16-key unit (16 rows x 128 B of one KV head) for K and V into a
+//               4-stage shared-memory ring guarded by mbarriers.
+//   warps 0..3  consumers: warp w takes unit w of each stage.  Scores for the
+//               G packed heads (M = 16 rows) come from mma.sync m16n8k16 bf16
+//               with fp32 accumulation, the online softmax runs in registers,
+//               and P*V reuses the score fragments as the A operand.
+// The four warps' states are merged through shared memory at the end and the
+// CTA writes either the final output (the sequence has one chunk) or an fp32
+// partial (o, lse) that the merge kernel combines.
+//
+// The kernel is HBM-bound: per key and KV head it moves 256 B and does
+// 2*G*64 MACs, which the tensor-core path hides completely.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn_sink {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kUnitsPerStage = kConsumerWarps;
+constexpr int kStages = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kUnitBytes = kUnitTokens * kHeadDim * 2;              // 2048
+constexpr int kStageBytes = 2 * kUnitsPerStage * kUnitBytes;         // 16 KB (K then V)
+constexpr int kRingBytes = kStages * kStageBytes;                    // 64 KB
+constexpr int kSmemBytes = kRingBytes + 1024 /*align slack*/ + 128 /*barriers*/;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct alignas(8) Barriers {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint32_t unit_ok[kStages];
+  int abort_word;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                        uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a 128B-swizzled tile
+// whose base is 1024-byte aligned (the layout TMA writes with SWIZZLE_128B).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Keep the bf16 halves of a B fragment whose key index is below n_valid.
+__device__ __forceinline__ uint32_t mask_keys(uint32_t v, int key_lo, int n_valid) {
+  uint32_t keep = (key_lo < n_valid ? 0x0000FFFFu : 0u) | (key_lo + 1 < n_valid ? 0xFFFF0000u : 0u);
+  return v & keep;
+}
+
+// Online-softmax state of one consumer warp for rows r0 = lane/4 and r1 = r0+8.
+struct WarpState {
+  float m0, m1;   // running max, log2 domain (quad-uniform)
+  float d0, d1;   // this thread's share of the running sum
+  float o[8][4];  // O fragments: [d tile][c0..c3]
+};
+
+// One 16-key unit: S = Q K^T, online softmax update, O += P V.
+template <bool kTwoRows>
+__device__ __forceinline__ void consume_unit(uint32_t k_base, uint32_t v_base, int n_valid,
+                                             const uint32_t (&qa)[4][4], float scale_log2,
+                                             WarpState& st) {
+  const int lane = threadIdx.x & 31;
+  float s[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+
+  {
+    const int mi = lane >> 3, ri = lane & 7;
+    const int key = (mi >> 1) * 8 + ri;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t b00, b01, b10, b11;
+      ldsm_x4(b00, b01, b10, b11, k_base + swz(key, 2 * ks + (mi & 1)));
+      mma_16816(s[0], qa[ks], b00, b01);
+      mma_16816(s[1], qa[ks], b10, b11);
+    }
+  }
+
+  const int kc = 2 * (lane & 3);
+  float x[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = nt * 8 + kc + (e & 1);
+      const bool row_ok = kTwoRows || e < 2;
+      x[nt][e] = (key < n_valid && row_ok) ? s[nt][e] * scale_log2 : -INFINITY;
+    }
+
+  float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  const float mn0 = fmaxf(st.m0, mx0);
+  const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float al0 = fast_exp2(st.m0 - mu0);
+  st.m0 = mn0;
+
+  float mn1 = -INFINITY, mu1 = 0.f, al1 = 1.f;
+  if (kTwoRows) {
+    float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    mn1 = fmaxf(st.m1, mx1);
+    mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    al1 = fast_exp2(st.m1 - mu1);
+    st.m1 = mn1;
+  }
+
+  float p[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    p[nt][0] = fast_exp2(x[nt][0] - mu0);
+    p[nt][1] = fast_exp2(x[nt][1] - mu0);
+    p[nt][2] = kTwoRows ? fast_exp2(x[nt][2] - mu1) : 0.f;
+    p[nt][3] = kTwoRows ? fast_exp2(x[nt][3] - mu1) : 0.f;
+  }
+  st.d0 = st.d0 * al0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+  if (kTwoRows) st.d1 = st.d1 * al1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+#pragma unroll
+  for (int dn = 0; dn < 8; ++dn) {
+    st.o[dn][0] *= al0;
+    st.o[dn][1] *= al0;
+    if (kTwoRows) {
+      st.o[dn][2] *= al1;
+      st.o[dn][3] *= al1;
+    }
+  }
+
+  uint32_t pa[4];
+  pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+  pa[1] = kTwoRows ? pack_bf16x2(p[0][2], p[0][3]) : 0u;
+  pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+  pa[3] = kTwoRows ? pack_bf16x2(p[1][2], p[1][3]) : 0u;
+
+  const int mi = lane >> 3, ri = lane & 7;
+  const int vkey = (mi & 1) * 8 + ri;
+#pragma unroll
+  for (int dp = 0; dp < 4; ++dp) {
+    uint32_t v0, v1, v2, v3;
+    ldsm_x4_trans(v0, v1, v2, v3, v_base + swz(vkey, 2 * dp + (mi >> 1)));
+    if (n_valid < kUnitTokens) {  // unused slots of a last page may hold anything
+      v0 = mask_keys(v0, kc, n_valid);
+      v1 = mask_keys(v1, 8 + kc, n_valid);
+      v2 = mask_keys(v2, kc, n_valid);
+      v3 = mask_keys(v3, 8 + kc, n_valid);
+    }
+    mma_16816(st.o[2 * dp], pa, v0, v1);
+    mma_16816(st.o[2 * dp + 1], pa, v2, v3);
+  }
+}
+
+template <bool kTwoRows>
+__global__ void __launch_bounds__(kThreads)
+    decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
+                        const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Barriers* bars = reinterpret_cast<Barriers*>(ring + kRingBytes);
+
+  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- chunk bounds in 16-key units (keys beyond the table row are not read)
+  const int kv_raw = a.kv_lens[b] > 0 ? a.kv_lens[b] : 0;
+  const int kv_len = min(kv_raw, a.bt_stride * a.page_size);
+  if (kv_len < kv_raw && threadIdx.x == 0 && c == 0 && g == 0 && a.err_flag)
+    atomicOr(a.err_flag, kFlagBadPage);
+  const int n_units_seq = (kv_len + kUnitTokens - 1) / kUnitTokens;
+  int u0, u1, n_chunks;
+  if (a.num_splits > 0) {
+    const int units_per_page = a.page_size / kUnitTokens;
+    const long long P = (kv_len + a.page_size - 1) / a.page_size;
+    const long long pb = (c * P) / a.num_splits, pe = ((c + 1) * P) / a.num_splits;
+    u0 = static_cast<int>(pb * units_per_page);
+    u1 = min(static_cast<int>(pe * units_per_page), n_units_seq);
+    n_chunks = a.num_splits;
+  } else {
+    n_chunks = max(1, (n_units_seq + a.chunk_units - 1) / a.chunk_units);
+    if (c >= n_chunks) return;
+    u0 = c * a.chunk_units;
+    u1 = min(u0 + a.chunk_units, n_units_seq);
+  }
+  if (u1 < u0) u1 = u0;
+  const int n_iters = (u1 - u0 + kUnitsPerStage - 1) / kUnitsPerStage;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], kConsumerWarps);
+    }
+    bars->abort_word = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&k_map);
+      tma_prefetch_map(&v_map);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    const int32_t* bt_row = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    int issued = 0;
+    for (int it = 0; it < n_iters; ++it) {
+      const int stage = it % kStages;
+      if (it >= kStages) {
+        const bool ready = mbar_wait(&bars->empty[stage], ((it / kStages) + 1) & 1,
+                                     &bars->abort_word, a.err_flag);
+        if (!__all_sync(0xffffffffu, ready)) break;
+      }
+      const int u = u0 + it * kUnitsPerStage + lane;
+      bool ok = false, bad = false;
+      int row = 0;
+      if (lane < kUnitsPerStage && u < u1) {
+        const int key0 = u * kUnitTokens;
+        const int phys = bt_row[key0 / a.page_size];
+        ok = phys >= 0 && phys < a.num_pages;
+        bad = !ok;
+        row = phys * a.page_size + (key0 % a.page_size);
+      }
+      const uint32_t ok_mask = __ballot_sync(0xffffffffu, ok);
+      if (__ballot_sync(0xffffffffu, bad) && lane == 0 && a.err_flag)
+        atomicOr(a.err_flag, kFlagBadPage);
+      if (lane == 0) {
+        bars->unit_ok[stage] = ok_mask;
+        mbar_arrive_expect_tx(&bars->full[stage], __popc(ok_mask) * 2 * kUnitBytes);
+      }
+      __syncwarp();
+      if (ok) {
+        uint8_t* st = ring + stage * kStageBytes;
+        tma_load_2d_hint(st + lane * kUnitBytes, &k_map, &bars->full[stage], g * kHeadDim, row,
+                         policy);
+        tma_load_2d_hint(st + (kUnitsPerStage + lane) * kUnitBytes, &v_map, &bars->full[stage],
+                         g * kHeadDim, row, policy);
+      }
+      issued = it + 1;
+    }
+    // Drain: every issued load lands before the CTA's shared memory goes away.
+    if (lane == 0) {
+      for (int it = max(0, issued - kStages); it < issued; ++it)
+        mbar_wait_drain(&bars->full[it % kStages], (it / kStages) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int r0 = lane >> 2, r1 = r0 + 8;
+  const int head0 = g * a.group;
+  uint32_t qa[4][4];
+  {
+    const __nv_bfloat16* qb =
+        reinterpret_cast<const __nv_bfloat16*>(a.q) + (static_cast<long long>(b) * a.Hq + head0) * kHeadDim;
+    const int col = 2 * (lane & 3);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const int d = 16 * ks + col;
+      qa[ks][0] = r0 < a.group ? *reinterpret_cast<const uint32_t*>(qb + r0 * kHeadDim + d) : 0u;
+      qa[ks][1] = r1 < a.group ? *reinterpret_cast<const uint32_t*>(qb + r1 * kHeadDim + d) : 0u;
+      qa[ks][2] = r0 < a.group ? *reinterpret_cast<const uint32_t*>(qb + r0 * kHeadDim + d + 8) : 0u;
+      qa[ks][3] = r1 < a.group ? *reinterpret_cast<const uint32_t*>(qb + r1 * kHeadDim + d + 8) : 0u;
+    }
+  }
+
+  WarpState st;
+  st.m0 = st.m1 = -INFINITY;
+  st.d0 = st.d1 = 0.f;
+#pragma unroll
+  for (int dn = 0; dn < 8; ++dn)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.o[dn][e] = 0.f;
+  if (c == 0 && warp == 0) {
+    // The sink enters as the initial running max with running sum 1, once.
+    st.m0 = r0 < a.group ? a.sinks[head0 + r0] * kLog2e : -INFINITY;
+    st.m1 = r1 < a.group ? a.sinks[head0 + r1] * kLog2e : -INFINITY;
+    st.d0 = (lane & 3) == 0 ? 1.f : 0.f;
+    st.d1 = (lane & 3) == 0 ? 1.f : 0.f;
+  }
+
+  for (int it = 0; it < n_iters; ++it) {
+    const int stage = it % kStages;
+    const bool ready = mbar_wait(&bars->full[stage], (it / kStages) & 1, &bars->abort_word, a.err_flag);
+    if (!__all_sync(0xffffffffu, ready)) break;
+    const int u = u0 + it * kUnitsPerStage + warp;
+    if (u < u1 && ((bars->unit_ok[stage] >> warp) & 1u)) {
+      const uint32_t k_base = smem_addr(ring + stage * kStageBytes + warp * kUnitBytes);
+      const uint32_t v_base = k_base + kUnitsPerStage * kUnitBytes;
+      const int n_valid = min(kUnitTokens, kv_len - u * kUnitTokens);
+      consume_unit<kTwoRows>(k_base, v_base, n_valid, qa, a.scale_log2, st);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->empty[stage]);
+  }
+
+  // ---- merge the four warps' states (shared memory reused after the ring drained)
+  st.d0 += __shfl_xor_sync(0xffffffffu, st.d0, 1);
+  st.d0 += __shfl_xor_sync(0xffffffffu, st.d0, 2);
+  st.d1 += __shfl_xor_sync(0xffffffffu, st.d1, 1);
+  st.d1 += __shfl_xor_sync(0xffffffffu, st.d1, 2);
+  named_barrier_sync(1, kConsumerWarps * 32);  // every consumer is done reading the ring
+
+  float* sm_o = reinterpret_cast<float*>(ring);                  // [warp][16][64]
+  float* sm_m = sm_o + kConsumerWarps * 16 * kHeadDim;          // [warp][16]
+  float* sm_d = sm_m + kConsumerWarps * 16;                     // [warp][16]
+  {
+    float* ow = sm_o + warp * 16 * kHeadDim;
+    const int col = 2 * (lane & 3);
+#pragma unroll
+    for (int dn = 0; dn < 8; ++dn) {
+      *reinterpret_cast<float2*>(ow + r0 * kHeadDim + dn * 8 + col) = make_float2(st.o[dn][0], st.o[dn][1]);
+      if (kTwoRows)
+        *reinterpret_cast<float2*>(ow + r1 * kHeadDim + dn * 8 + col) = make_float2(st.o[dn][2], st.o[dn][3]);
+    }
+    if ((lane & 3) == 0) {
+      sm_m[warp * 16 + r0] = st.m0;
+      sm_d[warp * 16 + r0] = st.d0;
+      sm_m[warp * 16 + r1] = st.m1;
+      sm_d[warp * 16 + r1] = st.d1;
+    }
+  }
+  named_barrier_sync(1, kConsumerWarps * 32);
+
+  const bool direct = n_chunks == 1;
+  for (int idx = threadIdx.x; idx < a.group * 16; idx += kConsumerWarps * 32) {
+    const int row = idx >> 4, d4 = (idx & 15) * 4;
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, sm_m[w * 16 + row]);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = sm_m[w * 16 + row];
+      const float sc = mw == -INFINITY ? 0.f : fast_exp2(mw - m);
+      den += sm_d[w * 16 + row] * sc;
+      const float4 ov = *reinterpret_cast<const float4*>(sm_o + (w * 16 + row) * kHeadDim + d4);
+      acc.x += ov.x * sc;
+      acc.y += ov.y * sc;
+      acc.z += ov.z * sc;
+      acc.w += ov.w * sc;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    const float lse = (den > 0.f && m != -INFINITY) ? (m + __log2f(den)) * kLn2 : -INFINITY;
+    const long long grow = static_cast<long long>(b) * a.Hq + head0 + row;
+    if (direct) {
+      uint2 packed;
+      packed.x = pack_bf16x2(acc.x, acc.y);
+      packed.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim + d4) = packed;
+      if (a.lse && d4 == 0) a.lse[grow] = lse;
+    } else {
+      *reinterpret_cast<float4*>(a.o_part + (grow * a.s_stride + c) * kHeadDim + d4) = acc;
+      if (d4 == 0) a.lse_part[grow * a.s_stride + c] = lse;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& k_map,
+                               const CUtensorMap& v_map, cudaStream_t stream) {
+  dim3 grid(a.max_chunks, a.Hkv, a.B);
+  if (a.group > 8) {
+    auto kern = decode_split_kernel<true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(k_map, v_map, a);
+  } else {
+    auto kern = decode_split_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(k_map, v_map, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace attn_sink

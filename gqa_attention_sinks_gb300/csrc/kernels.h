@@ -1,0 +1,96 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn_sink {
+
+constexpr int kHeadDim = 64;     // the only head dimension the kernels are built for
+constexpr int kUnitTokens = 16;  // keys per TMA box: one 16-row slice of a page
+
+// ------------------------------------------------------------- bf16 decode
+struct DecodeArgs {
+  const void* q;               // bf16 [B, Hq, 64]
+  const int32_t* kv_lens;      // [B]
+  const int32_t* block_table;  // [B, bt_stride]
+  const float* sinks;          // [Hq]
+  void* out;                   // bf16 [B, Hq, 64]   (rows that need no merge)
+  float* lse;                  // [B, Hq] or null
+  float* o_part;               // fp32 [B*Hq, s_stride, 64]
+  float* lse_part;             // fp32 [B*Hq, s_stride]
+  int32_t* err_flag;           // or null
+  int B, Hq, Hkv, group;
+  int bt_stride, page_size, num_pages;
+  float scale_log2;            // scale * log2(e)
+  int num_splits;              // > 0: fixed split count; 0: chunk_units mode
+  int chunk_units;             // 16-key units per chunk when num_splits == 0
+  int max_chunks;              // grid.x
+  int s_stride;                // partial slots per row in o_part / lse_part
+};
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& k_map,
+                               const CUtensorMap& v_map, cudaStream_t stream);
+
+// ------------------------------------------------------------- merge
+struct MergeArgs {
+  const float* o_part;    // [rows, s_stride, 64]
+  const float* lse_part;  // [rows, s_stride]
+  void* out;              // [rows, 64] bf16 or fp32
+  float* lse;             // [rows] or null
+  int rows, s_stride, num_parts;
+  int out_fp32;
+  // When kv_lens is set, row r belongs to sequence r / Hq and has
+  // max(1, ceil(ceil(kv_len/16) / chunk_units)) parts; rows with one part were
+  // written by the decode kernel and are skipped.
+  const int32_t* kv_lens;
+  int Hq, chunk_units;
+};
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------- fp32 path
+struct SimtArgs {
+  const float* q;              // [total_q, Hq, D]
+  const float* k_cache;        // [num_pages, page_size, Hkv, D]
+  const float* v_cache;
+  const int32_t* cu_seqlens_q; // [B+1] or null (decode: one query per sequence)
+  const int32_t* kv_lens;
+  const int32_t* block_table;
+  const float* sinks;
+  float* out;                  // [total_q, Hq, D] (num_splits == 1)
+  float* lse;                  // or null
+  float* o_part;               // [rows, num_splits, D]   (num_splits > 1)
+  float* lse_part;
+  int32_t* err_flag;
+  int B, total_q, Hq, Hkv, group;
+  int bt_stride, page_size, num_pages;
+  float scale_log2;
+  int causal;
+  int num_splits;
+};
+
+cudaError_t launch_simt_fp32(const SimtArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------- bf16 prefill
+struct PrefillArgs {
+  const int32_t* cu_seqlens_q;
+  const int32_t* kv_lens;
+  const int32_t* block_table;
+  const float* sinks;
+  void* out;                   // bf16 [total_q, Hq, 64]
+  float* lse;                  // [total_q, Hq] or null
+  int32_t* err_flag;
+  int B, total_q, max_q_len, Hq, Hkv, group;
+  int bt_stride, page_size, num_pages;
+  float scale_log2;
+  int causal;
+};
+
+cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
+                                const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                cudaStream_t stream);
+
+}  // namespace attn_sink

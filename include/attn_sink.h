@@ -1,0 +1,165 @@
+/*
+ * attn_sink.h -- C ABI of the GB300 (sm_103a) library for grouped-query
+ * attention with a learned per-head sink logit.
+ *
+ * The operation ("GPT-OSS pada Hari ke-0", section "Atensi Sink", and the model
+ * summary "Atensi: GQA dengan Sink Atensi"): every query head h owns a sink
+ * logit sink[h] that joins the softmax as one extra column next to the scaled
+ * query-key products,
+ *     z   = [ sink[h], scale * q . k_j  for every visible key j ],
+ *     out = sum_j softmax(z)[j] * v_j      (the sink column carries no value),
+ *     lse = ln( e^sink[h] + sum_j e^{scale q.k_j} ).
+ * The sink is a logit in the same units as scale*q.k (it is not scaled);
+ * sink = -inf gives ordinary attention.  The same section says that when the
+ * key sequence is split into chunks processed in parallel, the sink may be
+ * counted only in the first chunk; attn_sink_decode follows that rule and
+ * attn_sink_merge combines the chunks.
+ *
+ * Conventions shared by every call
+ *  - Pointers marked "device" are CUDA device addresses; "host" are host
+ *    addresses.  The caller owns every buffer.  The library never allocates,
+ *    frees, synchronises, or reads device memory back to the host, so every
+ *    call can be enqueued on a stream without a host round trip.
+ *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Layouts (row-major, innermost last):
+ *      q            [total_q, Hq, D]                 ragged by cu_seqlens_q
+ *      k_cache/v_cache [num_pages, page_size, Hkv, D]  paged cache
+ *      block_table  [B, block_table_stride] int32     logical -> physical page
+ *      sinks        [Hq] fp32 (may be -INFINITY; +inf/NaN are undefined)
+ *    Query head h reads KV head h / (Hq / Hkv).
+ *  - Query i (0-based) of a sequence with q_len queries and kv_len keys sits
+ *    at absolute position kv_len - q_len + i; with causal masking it sees keys
+ *    0..that position (bottom-right alignment: the queries are the last q_len
+ *    tokens of the sequence).  Keys at positions >= kv_len are never read.
+ *  - Supported shapes: D = 64; Hq % Hkv == 0 with group size Hq/Hkv a power
+ *    of two <= 16; page_size a multiple of 16 and <= 256 (bf16) or any
+ *    positive value (fp32).  Other shapes return ATTN_SINK_ERR_UNSUPPORTED.
+ *  - q, k_cache, v_cache and out must be 16-byte aligned.
+ *  - err_flag (device int32, may be NULL): the kernels OR bits into it and
+ *    never trap.  ATTN_SINK_FLAG_BAD_PAGE: a block_table entry outside
+ *    [0, num_pages) was met; that page's keys were skipped.
+ *    ATTN_SINK_FLAG_TIMEOUT: an internal pipeline wait exceeded its time
+ *    limit; the affected outputs are undefined.  The caller clears the flag.
+ *  - Errors found on the host return a status before anything is enqueued;
+ *    a failed launch returns ATTN_SINK_ERR_CUDA.
+ */
+#ifndef ATTN_SINK_H
+#define ATTN_SINK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_SINK_API __attribute__((visibility("default")))
+#else
+#define ATTN_SINK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_SINK_OK = 0,
+    ATTN_SINK_ERR_INVALID_ARG = 1,
+    ATTN_SINK_ERR_UNSUPPORTED = 2,
+    ATTN_SINK_ERR_WORKSPACE = 3,
+    ATTN_SINK_ERR_CUDA = 4
+} attn_sink_status;
+
+typedef enum {
+    ATTN_SINK_BF16 = 0, /* q/k/v/out bf16, fp32 accumulation, tensor cores */
+    ATTN_SINK_FP32 = 1  /* q/k/v/out fp32, fp32 arithmetic throughout     */
+} attn_sink_dtype;
+
+#define ATTN_SINK_FLAG_BAD_PAGE 1
+#define ATTN_SINK_FLAG_TIMEOUT 2
+
+/*
+ * Causal (or full) ragged prefill over a paged KV cache.
+ * ("GPT-OSS pada Hari ke-0", section "Atensi Sink": the prefill kernel
+ * template gains the sink parameter.)
+ *
+ *  q            device [total_q, Hq, D] dtype; sequence b owns rows
+ *               cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1.
+ *  k_cache, v_cache device [num_pages, page_size, Hkv, D] dtype.
+ *  cu_seqlens_q device int32 [B+1], non-decreasing, cu_seqlens_q[0] = 0,
+ *               cu_seqlens_q[B] = total_q.
+ *  kv_lens      device int32 [B]: keys of sequence b, new tokens included
+ *               (kv_len >= q_len when causal).
+ *  block_table  device int32 [B, block_table_stride]; entries for pages at or
+ *               beyond ceil(kv_len / page_size) are never read.
+ *  sinks        device fp32 [Hq].
+ *  out          device [total_q, Hq, D] dtype (written).
+ *  lse          device fp32 [total_q, Hq] natural-log LSE including the sink,
+ *               or NULL.
+ *  max_q_len    host upper bound of any sequence's q_len (sizes the grid).
+ *  scale        softmax scale applied to q.k (typically 1/sqrt(D)).
+ *  causal       1 = causal (bottom-right aligned), 0 = every key visible.
+ */
+ATTN_SINK_API attn_sink_status attn_sink_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                   const int32_t* block_table, int32_t block_table_stride,
+                                   const float* sinks, void* out, float* lse, int32_t B,
+                                   int32_t total_q, int32_t max_q_len, int32_t Hq, int32_t Hkv,
+                                   int32_t D, int32_t page_size, int32_t num_pages, float scale,
+                                   int32_t causal, attn_sink_dtype dtype, int32_t* err_flag,
+                                   void* stream);
+
+/*
+ * Paged-KV decode, one query token per sequence, optionally split along the
+ * key sequence ("GPT-OSS pada Hari ke-0", section "Atensi Sink": attention is
+ * parallelised over heads and along the KV length, and the sink is counted in
+ * the first chunk only).
+ *
+ *  q            device [B, Hq, D] dtype (the query of each sequence sits at
+ *               position kv_len - 1 and sees every key 0..kv_len-1).
+ *  kv_lens      device int32 [B] (0 allowed: out = 0, lse = sink).
+ *  out          device [B, Hq, D] dtype; lse device fp32 [B, Hq] or NULL.
+ *  num_splits   0: the library picks a chunk length in pages from B, Hkv and
+ *               block_table_stride; 1: no split; S > 1: chunk c of S covers
+ *               pages [floor(c*P/S), floor((c+1)*P/S)) with
+ *               P = ceil(kv_len/page_size).  S <= 256.
+ *  workspace    device scratch of at least attn_sink_decode_workspace_size()
+ *               bytes, 256-byte aligned (may be NULL when that size is 0).
+ *               Holds fp32 partial states between the split kernel and the
+ *               merge; no contents need to be preserved or initialised.
+ * The result does not depend on num_splits beyond fp32 rounding.
+ */
+ATTN_SINK_API attn_sink_status attn_sink_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* kv_lens, const int32_t* block_table,
+                                  int32_t block_table_stride, const float* sinks, void* out,
+                                  float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                  int32_t page_size, int32_t num_pages, float scale,
+                                  int32_t num_splits, attn_sink_dtype dtype, int32_t* err_flag,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_sink_decode needs for these arguments (0 when it needs
+ * none).  Pure host function. */
+ATTN_SINK_API size_t attn_sink_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                       int32_t block_table_stride, int32_t page_size,
+                                       int32_t num_splits);
+
+/*
+ * Log-sum-exp merge of S partial attention states per row.  For row r:
+ *     L = ln sum_c e^{lse_parts[r,c]},  out[r] = sum_c e^{lse_parts[r,c] - L} o_parts[r,c].
+ * It adds no sink: the sink lives inside whichever partial counted it (the
+ * first chunk, per "GPT-OSS pada Hari ke-0", section "Atensi Sink").  Rows
+ * whose partials are all -inf give out = 0 and L = -inf.
+ *
+ *  o_parts   device fp32 [rows, S, D], each partial normalised by its own sum.
+ *  lse_parts device fp32 [rows, S] natural-log LSE of each partial.
+ *  out       device [rows, D] dtype; lse_out device fp32 [rows] or NULL.
+ */
+ATTN_SINK_API attn_sink_status attn_sink_merge(const float* o_parts, const float* lse_parts, int32_t rows,
+                                 int32_t S, int32_t D, void* out, float* lse_out,
+                                 attn_sink_dtype dtype, void* stream);
+
+/* Static description of a status code. */
+ATTN_SINK_API const char* attn_sink_status_string(attn_sink_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SINK_H */
