@@ -34,6 +34,8 @@ SIGNATURES = {
     "attn_sink_decode": ([_vp] * 5 + [_i32, _vp, _vp, _vp] + [_i32] * 6 + [_f32, _i32, _i32, _vp,
                                                                          _vp, _sz, _vp], _i32),
     "attn_sink_decode_workspace_size": ([_i32] * 7, _sz),
+    "attn_sink_decode_static_scratch": ([_vp] * 5 + [_i32, _vp, _vp, _vp] + [_i32] * 6 +
+                                        [_f32, _i32, _i32, _vp, _vp], _i32),
     "attn_sink_merge": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp], _i32),
     "attn_sink_status_string": ([_i32], ctypes.c_char_p),
 }

@@ -155,6 +155,39 @@ ATTN_SINK_API attn_sink_status attn_sink_merge(const float* o_parts, const float
                                  int32_t S, int32_t D, void* out, float* lse_out,
                                  attn_sink_dtype dtype, void* stream);
 
+/*
+ * attn_sink_decode without a workspace argument, for callers that cannot
+ * allocate device memory: for example a host whose allocator owns all device
+ * memory and forbids libraries from calling cudaMalloc, or a latency-critical
+ * path that cannot afford cudaMalloc's implicit synchronisation.  (The pages
+ * describing the method have no counterpart to this; it is a library
+ * convenience.)
+ *
+ * Arguments, layouts and results are those of attn_sink_decode.  The split-KV
+ * partial states live in one library-owned static device array of
+ * ATTN_SINK_STATIC_SCRATCH_BYTES bytes, which every GPU that loads this part
+ * of the library holds until the process exits.  The caller still passes
+ * inputs and outputs; nothing is allocated per call.
+ *  - A call whose partials need more than ATTN_SINK_STATIC_SCRATCH_BYTES
+ *    (attn_sink_decode_workspace_size reports the need) returns
+ *    ATTN_SINK_ERR_WORKSPACE before enqueueing anything.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - All calls on a device share the array, which keeps the previous call's
+ *    contents.  Nothing in it needs clearing: every partial the merge reads is
+ *    written earlier in the same call.  Calls that overlap on the GPU (other
+ *    streams, or concurrent host threads) race on the array and must be
+ *    serialised by the caller.
+ */
+#define ATTN_SINK_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+ATTN_SINK_API attn_sink_status attn_sink_decode_static_scratch(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_lens,
+    const int32_t* block_table, int32_t block_table_stride, const float* sinks, void* out,
+    float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+    int32_t num_pages, float scale, int32_t num_splits, attn_sink_dtype dtype, int32_t* err_flag,
+    void* stream);
+
 /* Static description of a status code. */
 ATTN_SINK_API const char* attn_sink_status_string(attn_sink_status status);
 
