@@ -83,7 +83,8 @@ __device__ __forceinline__ uint32_t mask_keys(uint32_t v, int key_lo, int n_vali
 // Online-softmax state of one consumer warp for rows r0 = lane/4 and r1 = r0+8.
 struct WarpState {
   float m0, m1;   // running max, log2 domain (quad-uniform)
-  float d0, d1;   // this thread's share of the running sum
+  float d0, d1;   // this thread's share of the running sum of exact p (for lse)
+  float w0, w1;   // the same over the bf16-rounded p fed to P*V (normalises O)
   float o[8][4];  // O fragments: [d tile][c0..c3]
 };
 
@@ -149,8 +150,19 @@ __device__ __forceinline__ void consume_unit(uint32_t k_base, uint32_t v_base, i
     p[nt][2] = kTwoRows ? fast_exp2(x[nt][2] - mu1) : 0.f;
     p[nt][3] = kTwoRows ? fast_exp2(x[nt][3] - mu1) : 0.f;
   }
+  // P is rounded to bf16 for the P*V MMA.  w sums the same rounded values (so a
+  // row's weights sum to exactly 1); d sums the exact ones (for the lse).
+  uint32_t pa[4];
+  pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+  pa[1] = kTwoRows ? pack_bf16x2(p[0][2], p[0][3]) : 0u;
+  pa[2] = pack_bf16x2(p[1][0], p[1][1]);
+  pa[3] = kTwoRows ? pack_bf16x2(p[1][2], p[1][3]) : 0u;
   st.d0 = st.d0 * al0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-  if (kTwoRows) st.d1 = st.d1 * al1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+  st.w0 = st.w0 * al0 + (bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2]));
+  if (kTwoRows) {
+    st.d1 = st.d1 * al1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+    st.w1 = st.w1 * al1 + (bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3]));
+  }
 #pragma unroll
   for (int dn = 0; dn < 8; ++dn) {
     st.o[dn][0] *= al0;
@@ -160,12 +172,6 @@ __device__ __forceinline__ void consume_unit(uint32_t k_base, uint32_t v_base, i
       st.o[dn][3] *= al1;
     }
   }
-
-  uint32_t pa[4];
-  pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-  pa[1] = kTwoRows ? pack_bf16x2(p[0][2], p[0][3]) : 0u;
-  pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-  pa[3] = kTwoRows ? pack_bf16x2(p[1][2], p[1][3]) : 0u;
 
   const int mi = lane >> 3, ri = lane & 7;
   const int vkey = (mi & 1) * 8 + ri;
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(kThreads)
 
   WarpState st;
   st.m0 = st.m1 = -INFINITY;
-  st.d0 = st.d1 = 0.f;
+  st.d0 = st.d1 = st.w0 = st.w1 = 0.f;
 #pragma unroll
   for (int dn = 0; dn < 8; ++dn)
 #pragma unroll
@@ -309,8 +315,8 @@ __global__ void __launch_bounds__(kThreads)
     // The sink enters as the initial running max with running sum 1, once.
     st.m0 = r0 < a.group ? a.sinks[head0 + r0] * kLog2e : -INFINITY;
     st.m1 = r1 < a.group ? a.sinks[head0 + r1] * kLog2e : -INFINITY;
-    st.d0 = (lane & 3) == 0 ? 1.f : 0.f;
-    st.d1 = (lane & 3) == 0 ? 1.f : 0.f;
+    st.d0 = st.w0 = (lane & 3) == 0 ? 1.f : 0.f;
+    st.d1 = st.w1 = (lane & 3) == 0 ? 1.f : 0.f;
   }
 
   for (int it = 0; it < n_iters; ++it) {
@@ -333,11 +339,16 @@ __global__ void __launch_bounds__(kThreads)
   st.d0 += __shfl_xor_sync(0xffffffffu, st.d0, 2);
   st.d1 += __shfl_xor_sync(0xffffffffu, st.d1, 1);
   st.d1 += __shfl_xor_sync(0xffffffffu, st.d1, 2);
+  st.w0 += __shfl_xor_sync(0xffffffffu, st.w0, 1);
+  st.w0 += __shfl_xor_sync(0xffffffffu, st.w0, 2);
+  st.w1 += __shfl_xor_sync(0xffffffffu, st.w1, 1);
+  st.w1 += __shfl_xor_sync(0xffffffffu, st.w1, 2);
   named_barrier_sync(1, kConsumerWarps * 32);  // every consumer is done reading the ring
 
   float* sm_o = reinterpret_cast<float*>(ring);                  // [warp][16][64]
   float* sm_m = sm_o + kConsumerWarps * 16 * kHeadDim;          // [warp][16]
   float* sm_d = sm_m + kConsumerWarps * 16;                     // [warp][16]
+  float* sm_w = sm_d + kConsumerWarps * 16;                     // [warp][16]
   {
     float* ow = sm_o + warp * 16 * kHeadDim;
     const int col = 2 * (lane & 3);
@@ -350,8 +361,10 @@ __global__ void __launch_bounds__(kThreads)
     if ((lane & 3) == 0) {
       sm_m[warp * 16 + r0] = st.m0;
       sm_d[warp * 16 + r0] = st.d0;
+      sm_w[warp * 16 + r0] = st.w0;
       sm_m[warp * 16 + r1] = st.m1;
       sm_d[warp * 16 + r1] = st.d1;
+      sm_w[warp * 16 + r1] = st.w1;
     }
   }
   named_barrier_sync(1, kConsumerWarps * 32);
@@ -362,20 +375,21 @@ __global__ void __launch_bounds__(kThreads)
     float m = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, sm_m[w * 16 + row]);
-    float den = 0.f;
+    float den = 0.f, wden = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
       const float mw = sm_m[w * 16 + row];
       const float sc = mw == -INFINITY ? 0.f : fast_exp2(mw - m);
       den += sm_d[w * 16 + row] * sc;
+      wden += sm_w[w * 16 + row] * sc;
       const float4 ov = *reinterpret_cast<const float4*>(sm_o + (w * 16 + row) * kHeadDim + d4);
       acc.x += ov.x * sc;
       acc.y += ov.y * sc;
       acc.z += ov.z * sc;
       acc.w += ov.w * sc;
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const float inv = wden > 0.f ? 1.f / wden : 0.f;
     acc.x *= inv;
     acc.y *= inv;
     acc.z *= inv;

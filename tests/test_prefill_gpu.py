@@ -1,0 +1,134 @@
+"""GPU parity of the causal ragged prefill (tcgen05 / TMEM / TMA) against the oracle."""
+import math
+
+import numpy as np
+import pytest
+
+import workloads as W
+from _gpu import DeviceBatch, compare, oracle_problem
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill(gas, db, causal=None, **kw):
+    b = db.b
+    return gas.prefill(db.q, db.k, db.v, db.cu, db.kv_lens, db.bt, db.sinks,
+                       max_q_len=b.max_q_len, scale=b.scale,
+                       causal=b.causal if causal is None else causal, err_flag=db.err, **kw)
+
+
+def _batch(seed, q_lens, prefix=None, Hq=64, Hkv=8, sink_std=2.0, causal=True, dtype=W.BF16,
+           sinks=None):
+    rng = np.random.default_rng(seed)
+    q_lens = np.asarray(q_lens, np.int64)
+    pre = np.zeros_like(q_lens) if prefix is None else np.asarray(prefix, np.int64)
+    pool = W.make_pool(rng, q_lens + pre, Hkv, 64, 16, dtype)
+    s = W.sinks_normal(rng, Hq, sink_std) if sinks is None else np.asarray(sinks, np.float32)
+    q = W.make_queries(rng, int(q_lens.sum()), Hq, 64, dtype)
+    return W.batch_from_pool(pool, np.arange(len(q_lens)), q_lens, q, s, causal, dtype)
+
+
+def _check_all(gas, batch, what):
+    db = DeviceBatch(batch)
+    out, lse = _prefill(gas, db)
+    ref, ref_lse, _ = oracle_problem(batch).attention()
+    compare(out, lse, ref, ref_lse, what=what)
+    assert db.err.item() == 0, db.err.item()
+    return out, lse
+
+
+def test_prefill_ragged_self_attention(cuda_lib):
+    """Ragged lengths spanning several tiles plus short tails (1, 16, 33 tokens)."""
+    _check_all(cuda_lib, _batch(21, [200, 77, 1, 16, 33, 300]), "ragged causal")
+
+
+def test_prefill_with_prefix(cuda_lib):
+    """Chunked prefill: new tokens appended to an existing KV prefix (bottom-right causal)."""
+    _check_all(cuda_lib, _batch(22, [64, 100, 5, 130], prefix=[0, 300, 17, 1000]), "prefix")
+
+
+def test_prefill_non_causal(cuda_lib):
+    batch = _batch(23, [50, 129], prefix=[10, 60], causal=False)
+    _check_all(cuda_lib, batch, "non-causal")
+
+
+@pytest.mark.parametrize("group,Hkv", [(1, 4), (2, 4), (4, 2), (16, 2)])
+def test_prefill_group_sizes(cuda_lib, group, Hkv):
+    _check_all(cuda_lib, _batch(24, [70, 200], prefix=[0, 33], Hq=group * Hkv, Hkv=Hkv),
+               "group %d" % group)
+
+
+def test_prefill_sink_extremes(cuda_lib):
+    """Sinks -inf, -4, 0, 4, 8 and large: sink=-inf is plain attention, large sinks
+    push the output toward 0."""
+    sinks = np.array([-math.inf, -4, 0, 4, 8, 20, -math.inf, 8] * 8, np.float32)
+    _check_all(cuda_lib, _batch(25, [150, 40], prefix=[20, 0], sinks=sinks), "sink extremes")
+
+
+def test_prefill_outlier_keys(cuda_lib):
+    """1% of K rows scaled by 20 (logits in the hundreds): rescaling must stay exact."""
+    m = W.mixed_batch(seed=26, n_decode=1, decode_kv=(16, 16), n_prefill=3, prefill_new=160,
+                      prefix=(0, 700))
+    _check_all(cuda_lib, m["prefill"], "outliers")
+
+
+def test_prefill_fp32_tiny(cuda_lib):
+    """Tiny fp32 case: 2 seqs, Hq 8 / Hkv 2, q_len 16 over kv_len 64 (SIMT fp32 path)."""
+    t = W.tiny_prefill_decode()
+    _check_all(cuda_lib, t["prefill"], "fp32 tiny prefill")
+
+
+def test_prefill_page_table_bitwise_and_deterministic(cuda_lib):
+    batch = _batch(27, [130, 90], prefix=[40, 0])
+    rng = np.random.default_rng(27)
+    perm = rng.permutation(batch.num_pages)
+    inv = np.argsort(perm)
+    moved = W.Batch(batch.dtype, batch.q, batch.k_cache[perm], batch.v_cache[perm],
+                    batch.cu_seqlens_q, batch.kv_lens,
+                    np.where(batch.block_table >= 0, inv[np.maximum(batch.block_table, 0)],
+                             -1).astype(np.int32), batch.sinks, batch.scale)
+    a, b = DeviceBatch(batch), DeviceBatch(moved)
+    oa, la = _prefill(cuda_lib, a)
+    ob, lb = _prefill(cuda_lib, b)
+    oc, lc = _prefill(cuda_lib, a)
+    assert bool((oa == ob).all()) and bool((la == lb).all())
+    assert bool((oa == oc).all()) and bool((la == lc).all())
+
+
+def test_prefill_bad_page_sets_flag(cuda_lib):
+    batch = _batch(28, [100, 60], prefix=[50, 0])
+    batch.block_table[0, 2] = batch.num_pages + 1
+    db = DeviceBatch(batch)
+    out, lse = _prefill(cuda_lib, db)
+    assert db.err.item() & cuda_lib.FLAG_BAD_PAGE
+    assert not db.err.item() & cuda_lib.FLAG_TIMEOUT
+    ref, ref_lse, bad = oracle_problem(batch).attention()
+    assert bad > 0
+    compare(out, lse, ref, ref_lse, what="bad page")
+
+
+def test_prefill_gptoss_full_sampled(cuda_lib):
+    """8 x 4096 causal prefill, Hq 64 / Hkv 8: sampled rows incl. each sequence's ends."""
+    batch = W.gptoss_prefill()
+    db = DeviceBatch(batch)
+    out, lse = _prefill(cuda_lib, db)
+    rng = np.random.default_rng(29)
+    rows = W.sample_rows(rng, batch, 1536)
+    ends = np.concatenate([np.arange(t * batch.Hq, (t + 1) * batch.Hq)
+                           for c in batch.cu_seqlens_q[1:] for t in (c - 1, c - 4096)])
+    rows = np.unique(np.concatenate([rows, ends]))
+    ref, ref_lse, _ = oracle_problem(batch).attention(rows)
+    compare(out, lse, ref, ref_lse, rows=rows, what="gpt-oss prefill")
+    assert db.err.item() == 0
+
+
+def test_prefill_mixed_part_full(cuda_lib):
+    """Chunked-prefill half of the mixed batch: 4 x 512 new tokens over prefixes up to 16k."""
+    m = W.mixed_batch()
+    batch = m["prefill"]
+    db = DeviceBatch(batch)
+    out, lse = _prefill(cuda_lib, db)
+    rows = W.sample_rows(np.random.default_rng(30), batch, 2048)
+    ref, ref_lse, _ = oracle_problem(batch).attention(rows)
+    compare(out, lse, ref, ref_lse, rows=rows, what="mixed prefill")
+    assert db.err.item() == 0
