@@ -287,13 +287,20 @@ def run_ours(args, ws, rank, local):
             pstep()
             torch.cuda.synchronize()
             psteps = max(3, min(args.steps, 50))
+            sampler = ClockSampler(local)
+            sampler.start()
+            t_end = time.time() + args.clock_window
+            while time.time() < t_end:
+                pstep()
+                torch.cuda.synchronize()
             total_ms, per = timed(pstep, psteps, args.warmup, per_call=True)
+            pclocks = sampler.stop()
             pms = total_ms / psteps
             call_ms = float(np.mean(per))
             ach = flops / (call_ms * 1e-3) / 1e12
             peak = pk["bf16_tflops"]
             part.update({"value": round(ws * flops / (pms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                         "ms_per_step": round(pms, 4), "steps": psteps,
+                         "ms_per_step": round(pms, 4), "steps": psteps, "clocks": pclocks,
                          "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak,
                                       "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                                       "traffic": None, "peak_source": pk_kind}})
@@ -308,7 +315,8 @@ def run_ours(args, ws, rank, local):
                       "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                       "data": "synthetic (seeded normal q/k/v)",
                       "config": {"workload": part["workload"]},
-                      "roofline": part.get("roofline"), "gpu_launches": part.get("steps", 0)}
+                      "roofline": part.get("roofline"), "gpu_launches": part.get("steps", 0),
+                      "clocks": part.get("clocks")}
     return result
 
 

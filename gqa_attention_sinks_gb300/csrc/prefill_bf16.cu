@@ -26,9 +26,8 @@
 // and B), O += P V is 8 MMAs of 128x64x16 (A in TMEM, V MN-major).  Because P
 // has its own columns, a warpgroup hands S back (s_free) as soon as it has
 // loaded it, and the MMA thread issues S(j+1) before P*V(j): the next scores
-// are computed while the softmax of the current tile runs.  O is rescaled only
-// when a row's maximum grows by more than 2^8 (the final O/d is exact for any
-// reference maximum).
+// are computed while the softmax of the current tile runs.
+#include "exp2_poly.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -58,7 +57,12 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleLog2 = 8.f;
+// O is rescaled whenever a row's running maximum grows, so the largest p of a
+// row is exactly 1 and its bf16 rounding (for the P*V MMA) is exact.
+constexpr float kRescaleLog2 = 0.f;
+// Of every kPolyDen pairs of exponentials, kPolyNum go through the polynomial
+// on the FMA pipe and the rest through MUFU ex2, to balance the two pipes.
+constexpr int kPolyNum = 0, kPolyDen = 4;
 
 struct alignas(8) Bars {
   uint64_t q_full;
@@ -68,6 +72,7 @@ struct alignas(8) Bars {
   uint64_t s_free[kQTiles];   // the warpgroup has loaded S(j); S may be overwritten
   uint64_t p_ready[kQTiles];  // P(j) is in TMEM (and O rescaled)
   uint64_t pv_done[kQTiles];  // P*V(j) has completed: P may be overwritten, O is current
+  uint64_t exp_turn[kQTiles]; // warpgroup q may run its exponentials (token passed between them)
   uint64_t mma_done;
   uint32_t unit_ok[kStages];
   uint32_t tmem_base;
@@ -114,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_free[q], 4);   // one arrive per softmax warp
       mbar_init(&bars->p_ready[q], 4);
       mbar_init(&bars->pv_done[q], 1);
+      mbar_init(&bars->exp_turn[q], 4);   // one arrive per warp of the other warpgroup
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort_word = 0;
@@ -246,12 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long pos = static_cast<long long>(kv_len) - q_len + tok;
     const float scale_log2 = a.scale_log2;
     float m_run = a.sinks[head] * kLog2e;  // the sink is the initial running max ...
-    float d_run = 1.f;                     // ... with running sum e^0 = 1 (exact p: for lse)
-    float w_run = 1.f;                     // same sum over the bf16-rounded p (normalises O)
+    float d_run = 1.f;                     // ... with running sum e^0 = 1
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t s_taddr = tmem + lane_off + col_s(q);
     const uint32_t o_taddr = tmem + lane_off + col_o(q);
     const uint32_t p_taddr = tmem + lane_off + col_p(q);
+    // The two warpgroups take turns in the MUFU-heavy exponential loop, so that
+    // one computes exponentials while the other loads S, reduces and stores P.
+    // Warpgroup 1 hands warpgroup 0 the first turn.
+    if (q == 1 && lane == 0) mbar_arrive(&bars->exp_turn[0]);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int st = j % kStages;
@@ -305,17 +314,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (resc) {
         alpha = fast_exp2(m_run - m_new);
         d_run *= alpha;
-        w_run *= alpha;
         m_run = m_new;
       }
       const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-      // p = 2^(s*scale*log2e - m), rounded to bf16 for the P*V MMA.  One running
-      // sum adds the rounded values (so a row's weights sum to exactly 1), the
-      // other the exact ones (for the log-sum-exp).
+      // p = 2^(s*scale*log2e - m), rounded to bf16 for the P*V MMA; the running
+      // sum adds the unrounded p.
       const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
       const uint64_t negm2 = f2_pack(neg_m, neg_m);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint64_t ex2[2] = {0ull, 0ull};
+      uint64_t ex2[4] = {0ull, 0ull, 0ull, 0ull};
+      {
+        const bool turn = mbar_wait(&bars->exp_turn[q], j & 1, &bars->abort_word, a.err_flag);
+        ok = __all_sync(0xffffffffu, turn);
+        if (!ok) break;
+      }
       uint32_t p[2][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -325,13 +336,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      scale2, negm2);
           float x0, x1;
           f2_unpack(x2, x0, x1);
-          const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+          float e0, e1;
+          if (((c * 16 + i / 2) % kPolyDen) < kPolyNum) {
+            exp2_poly_pair(x0, x1, e0, e1);
+          } else {
+            e0 = fast_exp2(x0);
+            e1 = fast_exp2(x1);
+          }
           const uint32_t pk = pack_bf16x2(e0, e1);
           p[c >> 1][(c & 1) * 16 + i / 2] = pk;
-          acc2[(i >> 1) & 3] = f2_add(acc2[(i >> 1) & 3], f2_pack(bf16_lo(pk), bf16_hi(pk)));
-          ex2[(i >> 1) & 1] = f2_add(ex2[(i >> 1) & 1], f2_pack(e0, e1));
+          ex2[(i >> 1) & 3] = f2_add(ex2[(i >> 1) & 3], f2_pack(e0, e1));
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->exp_turn[q ^ 1]);  // pass the turn
       if (j > 0) {
         // P*V(j-1) must have consumed P(j-1) (and updated O) before P(j) and any
         // rescale of O go into TMEM.
@@ -343,11 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(p_taddr, p[0]);
       tmem_st32(p_taddr + 32, p[1]);
       {
-        const uint64_t t = f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3]));
         float lo, hi;
-        f2_unpack(t, lo, hi);
-        w_run += lo + hi;
-        f2_unpack(f2_add(ex2[0], ex2[1]), lo, hi);
+        f2_unpack(f2_add(f2_add(ex2[0], ex2[1]), f2_add(ex2[2], ex2[3])), lo, hi);
         d_run += lo + hi;
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -402,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before_sync();
     if (row_valid) {
-      const float inv = w_run > 0.f ? 1.f / w_run : 0.f;
+      const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
       const long long grow = static_cast<long long>(q_start + tok) * a.Hq + head;
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim);
 #pragma unroll
