@@ -43,12 +43,16 @@ constexpr int kUnitsPerTile = kKeys / kUnitTokens;            // 8
 constexpr int kUnitBytes = kUnitTokens * kHeadDim * 2;       // 2 KB
 constexpr int kTileBytes = kRows * kHeadDim * 2;             // 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;                  // K then V
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kThreads = 320;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kSoftmaxWarps = 4 * kQTiles;
+// One producer warp, then one MMA-issuing warp per Q tile (the first of them
+// also allocates TMEM).
+constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kQTiles);
+constexpr int kCtasPerSm = kQTiles == 1 ? 2 : 1;
+constexpr uint32_t kTmemCols = 256 * kQTiles;  // S, O and P of every Q tile
 __device__ __forceinline__ uint32_t col_s(int q) { return static_cast<uint32_t>(q) * 128u; }
-__device__ __forceinline__ uint32_t col_o(int q) { return 256u + static_cast<uint32_t>(q) * 64u; }
-__device__ __forceinline__ uint32_t col_p(int q) { return 384u + static_cast<uint32_t>(q) * 64u; }
+__device__ __forceinline__ uint32_t col_o(int q) { return 128u * kQTiles + static_cast<uint32_t>(q) * 64u; }
+__device__ __forceinline__ uint32_t col_p(int q) { return 192u * kQTiles + static_cast<uint32_t>(q) * 64u; }
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kQTiles * kTileBytes;
 constexpr int kOffBar = kOffKV + kStages * kStageBytes;
@@ -74,13 +78,13 @@ struct alignas(8) Bars {
   uint64_t pv_done[kQTiles];  // P*V(j) has completed: P may be overwritten, O is current
   uint64_t exp_turn[kQTiles]; // warpgroup q may run its exponentials (token passed between them)
   uint64_t mma_done;
-  uint32_t unit_ok[kStages];
+  uint32_t unit_ok[kStages];  // bit u: 16-key unit u of the stage's tile was loaded
   uint32_t tmem_base;
   int abort_word;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
@@ -112,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], kQTiles);  // released by every Q tile's P*V
     }
     for (int q = 0; q < kQTiles; ++q) {
       mbar_init(&bars->s_full[q], 1);
@@ -121,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->pv_done[q], 1);
       mbar_init(&bars->exp_turn[q], 4);   // one arrive per warp of the other warpgroup
     }
-    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->mma_done, kQTiles);
     bars->abort_word = 0;
     if (kv_len < kv_raw && g == 0 && blockIdx.z == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
     fence_barrier_init();
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ok_mask = __ballot_sync(0xffffffffu, ok);
       if (__ballot_sync(0xffffffffu, bad) && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
       if (lane == 0) {
-        bars->unit_ok[st] = ok_mask;
+        bars->unit_ok[st] = ok_mask;  // published by the arrive below (release)
         mbar_arrive_expect_tx(&bars->kv_full[st], __popc(ok_mask) * 2 * kUnitBytes);
       }
       __syncwarp();
@@ -189,8 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = max(0, issued - kStages); j < issued; ++j)
         mbar_wait_drain(&bars->kv_full[j % kStages], (j / kStages) & 1);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp >= kMmaWarp) {
     // ---------------------------------------------------------------- MMA
+    // Warp kMmaWarp + q issues every MMA of Q tile q, so the two tiles'
+    // pipelines never wait on each other.
+    const int q = warp - kMmaWarp;
     if (lane == 0 && n_kv > 0) {
       const uint32_t q_addr = smem_addr(base + kOffQ);
       auto issue_s = [&](int q, uint32_t k_addr) {
@@ -212,31 +219,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&bars->kv_full[0], 0, abort_word, a.err_flag);
       if (ok) {
         tc_fence_after_sync();
-        for (int q = 0; q < kQTiles; ++q) {
-          issue_s(q, kv_addr(0));
-          umma_commit(&bars->s_full[q]);
-        }
+        issue_s(q, kv_addr(0));
+        umma_commit(&bars->s_full[q]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         if (j + 1 < n_kv) {
           ok = mbar_wait(&bars->kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1, abort_word,
-                         a.err_flag);
-          for (int q = 0; q < kQTiles && ok; ++q) {
-            ok = mbar_wait(&bars->s_free[q], j & 1, abort_word, a.err_flag);
-            if (!ok) break;
-            tc_fence_after_sync();
-            issue_s(q, kv_addr(j + 1));
-            umma_commit(&bars->s_full[q]);
-          }
-        }
-        for (int q = 0; q < kQTiles && ok; ++q) {
-          ok = mbar_wait(&bars->p_ready[q], j & 1, abort_word, a.err_flag);
+                         a.err_flag) &&
+               mbar_wait(&bars->s_free[q], j & 1, abort_word, a.err_flag);
           if (!ok) break;
           tc_fence_after_sync();
-          issue_pv(q, j % kStages, j > 0);
-          umma_commit(&bars->pv_done[q]);
+          issue_s(q, kv_addr(j + 1));
+          umma_commit(&bars->s_full[q]);
         }
-        if (ok) umma_commit(&bars->kv_empty[j % kStages]);
+        ok = mbar_wait(&bars->p_ready[q], j & 1, abort_word, a.err_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_pv(q, j % kStages, j > 0);
+        umma_commit(&bars->pv_done[q]);
+        umma_commit(&bars->kv_empty[j % kStages]);
       }
       umma_commit(&bars->mma_done);
       mbar_wait_drain(&bars->mma_done, 0);  // no MMA may still write TMEM at dealloc
@@ -260,15 +261,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The two warpgroups take turns in the MUFU-heavy exponential loop, so that
     // one computes exponentials while the other loads S, reduces and stores P.
     // Warpgroup 1 hands warpgroup 0 the first turn.
-    if (q == 1 && lane == 0) mbar_arrive(&bars->exp_turn[0]);
+    if (kQTiles > 1 && q == 1 && lane == 0) mbar_arrive(&bars->exp_turn[0]);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int st = j % kStages;
       bool ready = mbar_wait(&bars->s_full[q], j & 1, &bars->abort_word, a.err_flag);
-      // (already complete; gives this thread acquire ordering on unit_ok and V)
+      // S(j) was computed from this stage, so its load phase has completed; the
+      // wait returns at once and orders the producer's unit_ok write before the read.
       ready = ready && mbar_wait(&bars->kv_full[st], (j / kStages) & 1, &bars->abort_word, a.err_flag);
       ok = __all_sync(0xffffffffu, ready);
       if (!ok) break;
+      const uint32_t uok = bars->unit_ok[st];
       tc_fence_after_sync();
       uint32_t s[4][32];
 #pragma unroll
@@ -279,7 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->s_free[q]);  // the MMA may now write S(j+1)
 
       const int key_base = j * kKeys;
-      const uint32_t uok = bars->unit_ok[st];
       const bool full = uok == 0xFFu && key_base + kKeys <= kv_len &&
                         (!a.causal || key_base + kKeys - 1 <= first_pos);
       if (!full) {
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
       const uint64_t negm2 = f2_pack(neg_m, neg_m);
       uint64_t ex2[4] = {0ull, 0ull, 0ull, 0ull};
-      {
+      if (kQTiles > 1) {
         const bool turn = mbar_wait(&bars->exp_turn[q], j & 1, &bars->abort_word, a.err_flag);
         ok = __all_sync(0xffffffffu, turn);
         if (!ok) break;
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->exp_turn[q ^ 1]);  // pass the turn
+      if (kQTiles > 1 && lane == 0) mbar_arrive(&bars->exp_turn[q ^ 1]);  // pass the turn
       if (j > 0) {
         // P*V(j-1) must have consumed P(j-1) (and updated O) before P(j) and any
         // rescale of O go into TMEM.
@@ -380,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before_sync();
-      if (q == 0) {
+      if (q == 0 && !full) {
         // Keys this tile does not hold (past kv_len, or a skipped page) may sit
         // over stale shared memory: their P is 0, but 0 * NaN is NaN, so clear V.
         const int col = r;
