@@ -1,32 +1,37 @@
 // Causal ragged prefill for bf16 sink attention on sm_103a: tcgen05 tensor
-// cores with TMEM accumulators, operands staged by TMA.
+// cores with TMEM accumulators, operands staged by TMA, persistent CTAs.
 //
 // "GPT-OSS pada Hari ke-0", section "Atensi Sink": the prefill kernel gains the
 // sink parameter; the online softmax starts its running maximum at the head's
-// sink value with running sum 1.  A prefill CTA scans every key a query row
-// sees, so every row starts from its sink.
+// sink value with running sum 1.  A work tile scans every key its query rows
+// see, so every row starts from its sink.
 //
-// Work unit (one CTA): sequence b, KV head g and a block of 256 query rows =
-// two Q tiles of 128 rows.  A Q tile packs 128/G consecutive query tokens x
-// the G query heads of KV group g (GQA packing), so each K/V tile is read once
-// per 2*128/G tokens of the whole group.
+// Work tile: sequence b, KV head g and a block of 256 query rows = two Q tiles
+// of 128 rows.  A Q tile packs 128/G consecutive query tokens x the G query
+// heads of KV group g (GQA packing), so each K/V tile is read once per 2*128/G
+// tokens of the whole group.  The grid has one CTA per SM; CTA c takes work
+// tiles c, c + gridDim.x, ... from a list ordered longest rows first (the last
+// query block of every sequence, then the one before, ...), so the rows with
+// the most keys start first and every CTA ends on short ones.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3  softmax for Q tile 0, warps 4-7 softmax for Q tile 1: one
 //              thread per row; S comes out of TMEM with tcgen05.ld, the row
 //              max/exp2/sum run in registers, P (bf16) goes back into TMEM in
-//              its own columns and feeds P*V as the A operand.
-//   warp 8     TMA producer: the two Q tiles once, then per 128-key tile eight
-//              16-row page slices of K and of V into a 3-stage ring.
-//   warp 9     allocates TMEM; lane 0 issues every tcgen05.mma and commit.
+//              its own columns and feeds P*V as the A operand.  The two
+//              warpgroups take turns in the exponential loop.
+//   warp 8     TMA producer: per work tile the two Q tiles (double-buffered),
+//              then per 128-key tile eight 16-row page slices of K and of V
+//              into a 3-stage ring.  It runs ahead across work tiles.
+//   warps 9-10 one MMA-issuing warp per Q tile (warp 9 also owns TMEM).
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,320), O1 [320,384),
 // P0 [384,448), P1 [448,512) (P as packed bf16 pairs).
 //
 // Per 128-key tile and Q tile: S = Q K^T is 4 MMAs of 128x128x16 (K-major A
-// and B), O += P V is 8 MMAs of 128x64x16 (A in TMEM, V MN-major).  Because P
-// has its own columns, a warpgroup hands S back (s_free) as soon as it has
-// loaded it, and the MMA thread issues S(j+1) before P*V(j): the next scores
-// are computed while the softmax of the current tile runs.
+// and B), O += P V is 8 MMAs of 128x64x16 (A in TMEM, V MN-major).  A
+// warpgroup hands S back (s_free) as soon as it has loaded it, so S(j+1) is
+// computed while the softmax of tile j runs.  Every barrier phase is counted
+// across work tiles, so the pipeline never drains between them.
 #include "exp2_poly.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -39,22 +44,23 @@ constexpr int kRows = 128;
 constexpr int kQTiles = 2;
 constexpr int kKeys = 128;
 constexpr int kStages = 3;
+constexpr int kQBufs = 2;
 constexpr int kUnitsPerTile = kKeys / kUnitTokens;            // 8
 constexpr int kUnitBytes = kUnitTokens * kHeadDim * 2;       // 2 KB
 constexpr int kTileBytes = kRows * kHeadDim * 2;             // 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;                  // K then V
+constexpr int kQBufBytes = kQTiles * kTileBytes;
 constexpr int kSoftmaxWarps = 4 * kQTiles;
 // One producer warp, then one MMA-issuing warp per Q tile (the first of them
 // also allocates TMEM).
 constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kQTiles);
-constexpr int kCtasPerSm = kQTiles == 1 ? 2 : 1;
 constexpr uint32_t kTmemCols = 256 * kQTiles;  // S, O and P of every Q tile
 __device__ __forceinline__ uint32_t col_s(int q) { return static_cast<uint32_t>(q) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int q) { return 128u * kQTiles + static_cast<uint32_t>(q) * 64u; }
 __device__ __forceinline__ uint32_t col_p(int q) { return 192u * kQTiles + static_cast<uint32_t>(q) * 64u; }
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kQTiles * kTileBytes;
+constexpr int kOffKV = kQBufs * kQBufBytes;
 constexpr int kOffBar = kOffKV + kStages * kStageBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
@@ -65,17 +71,20 @@ constexpr float kLn2 = 0.6931471805599453f;
 // row is exactly 1 and its bf16 rounding (for the P*V MMA) is exact.
 constexpr float kRescaleLog2 = 0.f;
 // Of every kPolyDen pairs of exponentials, kPolyNum go through the polynomial
-// on the FMA pipe and the rest through MUFU ex2, to balance the two pipes.
+// on the FMA pipe and the rest through MUFU ex2.  On GB300 MUFU ex2 issues
+// every 4 clocks per SMSP and the split measured slower, so it is off.
 constexpr int kPolyNum = 0, kPolyDen = 4;
 
 struct alignas(8) Bars {
-  uint64_t q_full;
+  uint64_t q_full[kQBufs];
+  uint64_t q_empty[kQBufs];   // both Q tiles' MMAs of the buffer's work tile are done
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full[kQTiles];   // S(j) is in TMEM
-  uint64_t s_free[kQTiles];   // the warpgroup has loaded S(j); S may be overwritten
-  uint64_t p_ready[kQTiles];  // P(j) is in TMEM (and O rescaled)
-  uint64_t pv_done[kQTiles];  // P*V(j) has completed: P may be overwritten, O is current
+  uint64_t s_full[kQTiles];   // S is in TMEM
+  uint64_t s_free[kQTiles];   // the warpgroup has loaded S; S may be overwritten
+  uint64_t p_ready[kQTiles];  // P is in TMEM (and O rescaled)
+  uint64_t pv_done[kQTiles];  // P*V has completed: P may be overwritten, O is current
+  uint64_t o_free[kQTiles];   // the warpgroup has read the work tile's final O
   uint64_t exp_turn[kQTiles]; // warpgroup q may run its exponentials (token passed between them)
   uint64_t mma_done;
   uint32_t unit_ok[kStages];  // bit u: 16-key unit u of the stage's tile was loaded
@@ -84,36 +93,56 @@ struct alignas(8) Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    prefill_kernel(const __grid_constant__ CUtensorMap q_map,
-                   const __grid_constant__ CUtensorMap k_map,
-                   const __grid_constant__ CUtensorMap v_map, const PrefillArgs a) {
-  const int g = blockIdx.x, b = blockIdx.y;
-  const int q_start = a.cu_seqlens_q[b];
-  const int q_len = a.cu_seqlens_q[b + 1] - q_start;
-  const int tok_per_tile = kRows / a.group;
-  const int tok_per_cta = kQTiles * tok_per_tile;
-  const int n_blocks = (q_len + tok_per_cta - 1) / tok_per_cta;
-  if (q_len <= 0 || static_cast<int>(blockIdx.z) >= n_blocks) return;
-  const int blk = n_blocks - 1 - static_cast<int>(blockIdx.z);  // longest rows first
-  const int tok0 = blk * tok_per_cta;
-  const int kv_raw = max(0, a.kv_lens[b]);
-  const int kv_len = min(kv_raw, a.bt_stride * a.page_size);
-  const long long first_pos = static_cast<long long>(kv_len) - q_len + tok0;
-  const long long last_pos = static_cast<long long>(kv_len) - q_len + min(tok0 + tok_per_cta, q_len) - 1;
-  long long key_end = kv_len;
+// A work tile, derived identically by every role from its linear index.
+struct WorkTile {
+  int b, g, q_start, q_len, tok0, kv_raw, kv_len, n_kv;
+  long long first_pos;  // absolute position of the tile's first query
+};
+
+__device__ __forceinline__ bool decode_tile(const PrefillArgs& a, long long t, int tok_per_cta,
+                                            WorkTile& w) {
+  const long long heads = static_cast<long long>(a.B) * a.Hkv;
+  const int r = static_cast<int>(t / heads);  // 0: last query block of each sequence
+  const int rem = static_cast<int>(t % heads);
+  w.b = rem / a.Hkv;
+  w.g = rem % a.Hkv;
+  w.q_start = a.cu_seqlens_q[w.b];
+  w.q_len = a.cu_seqlens_q[w.b + 1] - w.q_start;
+  const int n_blocks = w.q_len > 0 ? (w.q_len + tok_per_cta - 1) / tok_per_cta : 0;
+  if (r >= n_blocks) return false;
+  w.tok0 = (n_blocks - 1 - r) * tok_per_cta;
+  w.kv_raw = max(0, a.kv_lens[w.b]);
+  w.kv_len = min(w.kv_raw, a.bt_stride * a.page_size);  // keys beyond the table row are not read
+  w.first_pos = static_cast<long long>(w.kv_len) - w.q_len + w.tok0;
+  const long long last_pos =
+      static_cast<long long>(w.kv_len) - w.q_len + min(w.tok0 + tok_per_cta, w.q_len) - 1;
+  long long key_end = w.kv_len;
   if (a.causal && key_end > last_pos + 1) key_end = last_pos + 1;
   if (key_end < 0) key_end = 0;
-  const int n_kv = static_cast<int>((key_end + kKeys - 1) / kKeys);
+  w.n_kv = static_cast<int>((key_end + kKeys - 1) / kKeys);
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap q_map,
+                   const __grid_constant__ CUtensorMap k_map,
+                   const __grid_constant__ CUtensorMap v_map, const PrefillArgs a,
+                   const long long n_tiles) {
+  const int tok_per_tile = kRows / a.group;
+  const int tok_per_cta = kQTiles * tok_per_tile;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(base + kOffBar);
+  volatile int* abort_word = &bars->abort_word;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < kQBufs; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], kQTiles);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], kQTiles);  // released by every Q tile's P*V
@@ -123,11 +152,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&bars->s_free[q], 4);   // one arrive per softmax warp
       mbar_init(&bars->p_ready[q], 4);
       mbar_init(&bars->pv_done[q], 1);
-      mbar_init(&bars->exp_turn[q], 4);   // one arrive per warp of the other warpgroup
+      mbar_init(&bars->o_free[q], 4);
+      mbar_init(&bars->exp_turn[q], 4);  // one arrive per warp of the other warpgroup
     }
     mbar_init(&bars->mma_done, kQTiles);
     bars->abort_word = 0;
-    if (kv_len < kv_raw && g == 0 && blockIdx.z == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -145,99 +174,133 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       tma_prefetch_map(&q_map);
       tma_prefetch_map(&k_map);
       tma_prefetch_map(&v_map);
-      mbar_arrive_expect_tx(&bars->q_full, kQTiles * kTileBytes);
-      const uint64_t once = l2_policy_evict_first();  // each Q tile is read by one CTA
-      for (int q = 0; q < kQTiles; ++q)
-        tma_load_3d_hint(base + kOffQ + q * kTileBytes, &q_map, &bars->q_full, 0, g * a.group,
-                         q_start + tok0 + q * tok_per_tile, once);
     }
-    const uint64_t reuse = l2_policy_evict_last();    // K/V tiles serve every later query block
-    const int32_t* bt_row = a.block_table + static_cast<long long>(b) * a.bt_stride;
-    int issued = 0;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j % kStages;
-      if (j >= kStages) {
-        const bool ready = mbar_wait(&bars->kv_empty[st], ((j / kStages) + 1) & 1,
-                                     &bars->abort_word, a.err_flag);
-        if (!__all_sync(0xffffffffu, ready)) break;
+    const uint64_t once = l2_policy_evict_first();   // each Q tile is read by one CTA
+    const uint64_t reuse = l2_policy_evict_last();   // K/V tiles serve every later query block
+    int qw = 0, kv_it = 0;
+    bool ok = true;
+    for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      WorkTile w;
+      if (!decode_tile(a, t, tok_per_cta, w)) continue;
+      if (w.kv_len < w.kv_raw && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
+      if (w.n_kv == 0) continue;
+      const int qb = qw % kQBufs;
+      if (qw >= kQBufs) {
+        const bool ready = mbar_wait(&bars->q_empty[qb], ((qw / kQBufs) + 1) & 1, abort_word, a.err_flag);
+        ok = __all_sync(0xffffffffu, ready);
+        if (!ok) break;
       }
-      bool ok = false, bad = false;
-      int row = 0;
-      if (lane < kUnitsPerTile) {
-        const int key0 = (j * kUnitsPerTile + lane) * kUnitTokens;
-        if (key0 < kv_len) {
-          const int phys = bt_row[key0 / a.page_size];
-          ok = phys >= 0 && phys < a.num_pages;
-          bad = !ok;
-          row = phys * a.page_size + key0 % a.page_size;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full[qb], kQBufBytes);
+        for (int q = 0; q < kQTiles; ++q)
+          tma_load_3d_hint(base + kOffQ + qb * kQBufBytes + q * kTileBytes, &q_map, &bars->q_full[qb],
+                           0, w.g * a.group, w.q_start + w.tok0 + q * tok_per_tile, once);
+      }
+      ++qw;
+      const int32_t* bt_row = a.block_table + static_cast<long long>(w.b) * a.bt_stride;
+      for (int j = 0; j < w.n_kv; ++j, ++kv_it) {
+        const int st = kv_it % kStages;
+        if (kv_it >= kStages) {
+          const bool ready = mbar_wait(&bars->kv_empty[st], ((kv_it / kStages) + 1) & 1, abort_word,
+                                       a.err_flag);
+          ok = __all_sync(0xffffffffu, ready);
+          if (!ok) break;
+        }
+        bool unit_ok = false, bad = false;
+        int row = 0;
+        if (lane < kUnitsPerTile) {
+          const int key0 = (j * kUnitsPerTile + lane) * kUnitTokens;
+          if (key0 < w.kv_len) {
+            const int phys = bt_row[key0 / a.page_size];
+            unit_ok = phys >= 0 && phys < a.num_pages;
+            bad = !unit_ok;
+            row = phys * a.page_size + key0 % a.page_size;
+          }
+        }
+        const uint32_t ok_mask = __ballot_sync(0xffffffffu, unit_ok);
+        if (__ballot_sync(0xffffffffu, bad) && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
+        if (lane == 0) {
+          bars->unit_ok[st] = ok_mask;  // published by the arrive below (release)
+          mbar_arrive_expect_tx(&bars->kv_full[st], __popc(ok_mask) * 2 * kUnitBytes);
+        }
+        __syncwarp();
+        if (unit_ok) {
+          uint8_t* stage = base + kOffKV + st * kStageBytes;
+          tma_load_2d_hint(stage + lane * kUnitBytes, &k_map, &bars->kv_full[st], w.g * kHeadDim,
+                           row, reuse);
+          tma_load_2d_hint(stage + kTileBytes + lane * kUnitBytes, &v_map, &bars->kv_full[st],
+                           w.g * kHeadDim, row, reuse);
         }
       }
-      const uint32_t ok_mask = __ballot_sync(0xffffffffu, ok);
-      if (__ballot_sync(0xffffffffu, bad) && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
-      if (lane == 0) {
-        bars->unit_ok[st] = ok_mask;  // published by the arrive below (release)
-        mbar_arrive_expect_tx(&bars->kv_full[st], __popc(ok_mask) * 2 * kUnitBytes);
-      }
-      __syncwarp();
-      if (ok) {
-        uint8_t* stage = base + kOffKV + st * kStageBytes;
-        tma_load_2d_hint(stage + lane * kUnitBytes, &k_map, &bars->kv_full[st], g * kHeadDim,
-                         row, reuse);
-        tma_load_2d_hint(stage + kTileBytes + lane * kUnitBytes, &v_map, &bars->kv_full[st],
-                         g * kHeadDim, row, reuse);
-      }
-      issued = j + 1;
     }
     if (lane == 0) {  // every issued copy lands before the CTA leaves
-      mbar_wait_drain(&bars->q_full, 0);
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        mbar_wait_drain(&bars->kv_full[j % kStages], (j / kStages) & 1);
+      for (int i = max(0, qw - kQBufs); i < qw; ++i)
+        mbar_wait_drain(&bars->q_full[i % kQBufs], (i / kQBufs) & 1);
+      for (int i = max(0, kv_it - kStages); i < kv_it; ++i)
+        mbar_wait_drain(&bars->kv_full[i % kStages], (i / kStages) & 1);
     }
   } else if (warp >= kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     // Warp kMmaWarp + q issues every MMA of Q tile q, so the two tiles'
     // pipelines never wait on each other.
     const int q = warp - kMmaWarp;
-    if (lane == 0 && n_kv > 0) {
-      const uint32_t q_addr = smem_addr(base + kOffQ);
-      auto issue_s = [&](int q, uint32_t k_addr) {
+    if (lane == 0) {
+      auto issue_s = [&](uint32_t q_addr, uint32_t k_addr) {
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          umma_ss(tmem + col_s(q), smem_desc_sw128(q_addr + q * kTileBytes + kk * 32, 16, 1024),
+          umma_ss(tmem + col_s(q), smem_desc_sw128(q_addr + kk * 32, 16, 1024),
                   smem_desc_sw128(k_addr + kk * 32, 16, 1024), kIdescS, kk > 0);
       };
-      auto issue_pv = [&](int q, int st, bool acc) {
+      auto issue_pv = [&](int st, bool acc) {
         const uint32_t v_addr = smem_addr(base + kOffKV + st * kStageBytes + kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           umma_ts(tmem + col_o(q), tmem + col_p(q) + kk * 8,
                   smem_desc_sw128(v_addr + kk * 2048, 8192, 1024), kIdescPV, acc || kk > 0);
       };
-      auto kv_addr = [&](int j) { return smem_addr(base + kOffKV + (j % kStages) * kStageBytes); };
-      volatile int* abort_word = &bars->abort_word;
-      bool ok = mbar_wait(&bars->q_full, 0, abort_word, a.err_flag) &&
-                mbar_wait(&bars->kv_full[0], 0, abort_word, a.err_flag);
-      if (ok) {
-        tc_fence_after_sync();
-        issue_s(q, kv_addr(0));
-        umma_commit(&bars->s_full[q]);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          ok = mbar_wait(&bars->kv_full[(j + 1) % kStages], ((j + 1) / kStages) & 1, abort_word,
-                         a.err_flag) &&
-               mbar_wait(&bars->s_free[q], j & 1, abort_word, a.err_flag);
-          if (!ok) break;
-          tc_fence_after_sync();
-          issue_s(q, kv_addr(j + 1));
-          umma_commit(&bars->s_full[q]);
-        }
-        ok = mbar_wait(&bars->p_ready[q], j & 1, abort_word, a.err_flag);
+      auto kv_addr = [&](int it) { return smem_addr(base + kOffKV + (it % kStages) * kStageBytes); };
+      int qw = 0, kv_it = 0, it = 0, ow = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        WorkTile w;
+        if (!decode_tile(a, t, tok_per_cta, w) || w.n_kv == 0) continue;
+        const int qb = qw % kQBufs;
+        const uint32_t q_addr = smem_addr(base + kOffQ + qb * kQBufBytes + q * kTileBytes);
+        // Q loaded, the first K/V tile in, and the previous S read out of TMEM.
+        ok = mbar_wait(&bars->q_full[qb], (qw / kQBufs) & 1, abort_word, a.err_flag) &&
+             mbar_wait(&bars->kv_full[kv_it % kStages], (kv_it / kStages) & 1, abort_word, a.err_flag) &&
+             (it == 0 || mbar_wait(&bars->s_free[q], (it - 1) & 1, abort_word, a.err_flag));
         if (!ok) break;
         tc_fence_after_sync();
-        issue_pv(q, j % kStages, j > 0);
-        umma_commit(&bars->pv_done[q]);
-        umma_commit(&bars->kv_empty[j % kStages]);
+        issue_s(q_addr, kv_addr(kv_it));
+        umma_commit(&bars->s_full[q]);
+        for (int j = 0; j < w.n_kv; ++j) {
+          const int cur = kv_it + j, u = it + j;
+          if (j + 1 < w.n_kv) {
+            ok = mbar_wait(&bars->kv_full[(cur + 1) % kStages], ((cur + 1) / kStages) & 1, abort_word,
+                           a.err_flag) &&
+                 mbar_wait(&bars->s_free[q], u & 1, abort_word, a.err_flag);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_s(q_addr, kv_addr(cur + 1));
+            umma_commit(&bars->s_full[q]);
+          }
+          // The first P*V of a work tile overwrites O: the previous tile's O must
+          // have been read out by then.
+          ok = mbar_wait(&bars->p_ready[q], u & 1, abort_word, a.err_flag) &&
+               (j > 0 || ow == 0 || mbar_wait(&bars->o_free[q], (ow - 1) & 1, abort_word, a.err_flag));
+          if (!ok) break;
+          tc_fence_after_sync();
+          issue_pv(cur % kStages, j > 0);
+          umma_commit(&bars->pv_done[q]);
+          umma_commit(&bars->kv_empty[cur % kStages]);
+        }
+        if (!ok) break;
+        umma_commit(&bars->q_empty[qb]);
+        ++qw;
+        kv_it += w.n_kv;
+        it += w.n_kv;
+        ++ow;
       }
       umma_commit(&bars->mma_done);
       mbar_wait_drain(&bars->mma_done, 0);  // no MMA may still write TMEM at dealloc
@@ -247,13 +310,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int q = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
-    const int tok = tok0 + q * tok_per_tile + r / a.group;
-    const int head = g * a.group + r % a.group;
-    const bool row_valid = tok < q_len;
-    const long long pos = static_cast<long long>(kv_len) - q_len + tok;
     const float scale_log2 = a.scale_log2;
-    float m_run = a.sinks[head] * kLog2e;  // the sink is the initial running max ...
-    float d_run = 1.f;                     // ... with running sum e^0 = 1
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t s_taddr = tmem + lane_off + col_s(q);
     const uint32_t o_taddr = tmem + lane_off + col_o(q);
@@ -262,178 +319,192 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // one computes exponentials while the other loads S, reduces and stores P.
     // Warpgroup 1 hands warpgroup 0 the first turn.
     if (kQTiles > 1 && q == 1 && lane == 0) mbar_arrive(&bars->exp_turn[0]);
+    int kv_it = 0, it = 0;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j % kStages;
-      bool ready = mbar_wait(&bars->s_full[q], j & 1, &bars->abort_word, a.err_flag);
-      // S(j) was computed from this stage, so its load phase has completed; the
-      // wait returns at once and orders the producer's unit_ok write before the read.
-      ready = ready && mbar_wait(&bars->kv_full[st], (j / kStages) & 1, &bars->abort_word, a.err_flag);
-      ok = __all_sync(0xffffffffu, ready);
-      if (!ok) break;
-      const uint32_t uok = bars->unit_ok[st];
-      tc_fence_after_sync();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_taddr + 32 * c, s[c]);
-      tmem_wait_ld();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free[q]);  // the MMA may now write S(j+1)
-
-      const int key_base = j * kKeys;
-      const bool full = uok == 0xFFu && key_base + kKeys <= kv_len &&
-                        (!a.causal || key_base + kKeys - 1 <= first_pos);
-      if (!full) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = 32 * c + i;
-            const int key = key_base + col;
-            const bool valid = key < kv_len && ((uok >> (col / kUnitTokens)) & 1u) &&
-                               (!a.causal || key <= pos);
-            if (!valid) s[c][i] = __float_as_uint(-INFINITY);
-          }
-      }
-      // Row max: eight independent chains of 3-input max.
-      float mx;
-      {
-        float ch[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t* v = &s[k >> 1][(k & 1) * 16];
-          float acc = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-#pragma unroll
-          for (int i = 3; i < 15; i += 2) acc = max3f(acc, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-          ch[k] = fmaxf(acc, __uint_as_float(v[15]));
-        }
-        mx = max3f(max3f(ch[0], ch[1], ch[2]), max3f(ch[3], ch[4], ch[5]), fmaxf(ch[6], ch[7]));
-      }
-      const float m_new = fmaxf(m_run, mx * scale_log2);
-      const bool resc = m_new > m_run + kRescaleLog2;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = fast_exp2(m_run - m_new);
-        d_run *= alpha;
-        m_run = m_new;
-      }
-      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-      // p = 2^(s*scale*log2e - m), rounded to bf16 for the P*V MMA; the running
-      // sum adds the unrounded p.
-      const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-      const uint64_t negm2 = f2_pack(neg_m, neg_m);
-      uint64_t ex2[4] = {0ull, 0ull, 0ull, 0ull};
-      if (kQTiles > 1) {
-        const bool turn = mbar_wait(&bars->exp_turn[q], j & 1, &bars->abort_word, a.err_flag);
-        ok = __all_sync(0xffffffffu, turn);
+    for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      WorkTile w;
+      if (!decode_tile(a, t, tok_per_cta, w)) continue;
+      const int tok = w.tok0 + q * tok_per_tile + r / a.group;
+      const int head = w.g * a.group + r % a.group;
+      const bool row_valid = tok < w.q_len;
+      const long long pos = static_cast<long long>(w.kv_len) - w.q_len + tok;
+      float m_run = a.sinks[head] * kLog2e;  // the sink is the initial running max ...
+      float d_run = 1.f;                     // ... with running sum e^0 = 1
+      for (int j = 0; j < w.n_kv; ++j) {
+        const int cur = kv_it + j, u = it + j;
+        const int st = cur % kStages;
+        bool ready = mbar_wait(&bars->s_full[q], u & 1, abort_word, a.err_flag);
+        // S was computed from this stage, so its load phase has completed; the
+        // wait returns at once and orders the producer's unit_ok write before the read.
+        ready = ready && mbar_wait(&bars->kv_full[st], (cur / kStages) & 1, abort_word, a.err_flag);
+        ok = __all_sync(0xffffffffu, ready);
         if (!ok) break;
-      }
-      uint32_t p[2][32];
+        const uint32_t uok = bars->unit_ok[st];
+        tc_fence_after_sync();
+        uint32_t s[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_taddr + 32 * c, s[c]);
+        tmem_wait_ld();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[q]);  // the MMA may now write the next S
+
+        const int key_base = j * kKeys;
+        const bool full = uok == 0xFFu && key_base + kKeys <= w.kv_len &&
+                          (!a.causal || key_base + kKeys - 1 <= w.first_pos);
+        if (!full) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])),
-                                     scale2, negm2);
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          float e0, e1;
-          if (((c * 16 + i / 2) % kPolyDen) < kPolyNum) {
-            exp2_poly_pair(x0, x1, e0, e1);
-          } else {
-            e0 = fast_exp2(x0);
-            e1 = fast_exp2(x1);
-          }
-          const uint32_t pk = pack_bf16x2(e0, e1);
-          p[c >> 1][(c & 1) * 16 + i / 2] = pk;
-          ex2[(i >> 1) & 3] = f2_add(ex2[(i >> 1) & 3], f2_pack(e0, e1));
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int col = 32 * c + i;
+              const int key = key_base + col;
+              const bool valid = key < w.kv_len && ((uok >> (col / kUnitTokens)) & 1u) &&
+                                 (!a.causal || key <= pos);
+              if (!valid) s[c][i] = __float_as_uint(-INFINITY);
+            }
         }
+        // Row max: eight independent chains of 3-input max.
+        float mx;
+        {
+          float ch[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t* v = &s[k >> 1][(k & 1) * 16];
+            float acc = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+            for (int i = 3; i < 15; i += 2) acc = max3f(acc, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+            ch[k] = fmaxf(acc, __uint_as_float(v[15]));
+          }
+          mx = max3f(max3f(ch[0], ch[1], ch[2]), max3f(ch[3], ch[4], ch[5]), fmaxf(ch[6], ch[7]));
+        }
+        const float m_new = fmaxf(m_run, mx * scale_log2);
+        const bool resc = m_new > m_run + kRescaleLog2;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = fast_exp2(m_run - m_new);
+          d_run *= alpha;
+          m_run = m_new;
+        }
+        const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+        // p = 2^(s*scale*log2e - m), rounded to bf16 for the P*V MMA; the running
+        // sum adds the unrounded p.
+        const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+        const uint64_t negm2 = f2_pack(neg_m, neg_m);
+        uint64_t ex2[4] = {0ull, 0ull, 0ull, 0ull};
+        if (kQTiles > 1) {
+          const bool turn = mbar_wait(&bars->exp_turn[q], u & 1, abort_word, a.err_flag);
+          ok = __all_sync(0xffffffffu, turn);
+          if (!ok) break;
+        }
+        uint32_t p[2][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1])),
+                                       scale2, negm2);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            float e0, e1;
+            if (((c * 16 + i / 2) % kPolyDen) < kPolyNum) {
+              exp2_poly_pair(x0, x1, e0, e1);
+            } else {
+              e0 = fast_exp2(x0);
+              e1 = fast_exp2(x1);
+            }
+            const uint32_t pk = pack_bf16x2(e0, e1);
+            p[c >> 1][(c & 1) * 16 + i / 2] = pk;
+            ex2[(i >> 1) & 3] = f2_add(ex2[(i >> 1) & 3], f2_pack(e0, e1));
+          }
+        }
+        __syncwarp();
+        if (kQTiles > 1 && lane == 0) mbar_arrive(&bars->exp_turn[q ^ 1]);  // pass the turn
+        if (u > 0) {
+          // The previous P*V must have consumed P (and updated O) before this P
+          // and any rescale of O go into TMEM.
+          const bool done = mbar_wait(&bars->pv_done[q], (u - 1) & 1, abort_word, a.err_flag);
+          ok = __all_sync(0xffffffffu, done);
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
+        tmem_st32(p_taddr, p[0]);
+        tmem_st32(p_taddr + 32, p[1]);
+        {
+          float lo, hi;
+          f2_unpack(f2_add(f2_add(ex2[0], ex2[1]), f2_add(ex2[2], ex2[3])), lo, hi);
+          d_run += lo + hi;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          // (At j == 0 the first P*V of the work tile overwrites O instead.)
+          uint32_t o[2][32];
+          tmem_ld32(o_taddr, o[0]);
+          tmem_ld32(o_taddr + 32, o[1]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[h][i] = __float_as_uint(__uint_as_float(o[h][i]) * alpha);
+          tmem_st32(o_taddr, o[0]);
+          tmem_st32(o_taddr + 32, o[1]);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        if (q == 0 && !full) {
+          // Keys this tile does not hold (past kv_len, or a skipped page) may sit
+          // over stale shared memory: their P is 0, but 0 * NaN is NaN, so clear V.
+          const int col = r;
+          const bool held = key_base + col < w.kv_len && ((uok >> (col / kUnitTokens)) & 1u);
+          if (!held) {
+            uint4* vrow = reinterpret_cast<uint4*>(base + kOffKV + st * kStageBytes + kTileBytes + col * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_ready[q]);
       }
-      __syncwarp();
-      if (kQTiles > 1 && lane == 0) mbar_arrive(&bars->exp_turn[q ^ 1]);  // pass the turn
-      if (j > 0) {
-        // P*V(j-1) must have consumed P(j-1) (and updated O) before P(j) and any
-        // rescale of O go into TMEM.
-        const bool done = mbar_wait(&bars->pv_done[q], (j - 1) & 1, &bars->abort_word, a.err_flag);
-        ok = __all_sync(0xffffffffu, done);
+      if (!ok) break;
+
+      // -------------------------------------------------------------- epilogue
+      uint32_t o[2][32];
+      if (w.n_kv > 0) {
+        const bool ready = mbar_wait(&bars->pv_done[q], (it + w.n_kv - 1) & 1, abort_word, a.err_flag);
+        ok = __all_sync(0xffffffffu, ready);
         if (!ok) break;
         tc_fence_after_sync();
-      }
-      tmem_st32(p_taddr, p[0]);
-      tmem_st32(p_taddr + 32, p[1]);
-      {
-        float lo, hi;
-        f2_unpack(f2_add(f2_add(ex2[0], ex2[1]), f2_add(ex2[2], ex2[3])), lo, hi);
-        d_run += lo + hi;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        // P*V(j-1) has completed (pv_done above); rescale O in place.
-        uint32_t o[2][32];
         tmem_ld32(o_taddr, o[0]);
         tmem_ld32(o_taddr + 32, o[1]);
         tmem_wait_ld();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_free[q]);  // the next work tile may overwrite O
+      } else {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[h][i] = __float_as_uint(__uint_as_float(o[h][i]) * alpha);
-        tmem_st32(o_taddr, o[0]);
-        tmem_st32(o_taddr + 32, o[1]);
+          for (int i = 0; i < 32; ++i) o[h][i] = 0u;
       }
-      tmem_wait_st();
-      tc_fence_before_sync();
-      if (q == 0 && !full) {
-        // Keys this tile does not hold (past kv_len, or a skipped page) may sit
-        // over stale shared memory: their P is 0, but 0 * NaN is NaN, so clear V.
-        const int col = r;
-        const bool held = key_base + col < kv_len && ((uok >> (col / kUnitTokens)) & 1u);
-        if (!held) {
-          uint4* vrow = reinterpret_cast<uint4*>(base + kOffKV + st * kStageBytes + kTileBytes + col * 128);
+      if (row_valid) {
+        const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
+        const long long grow = static_cast<long long>(w.q_start + tok) * a.Hq + head;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0u, 0u, 0u, 0u);
-          fence_proxy_async_smem();
+        for (int v = 0; v < 8; ++v) {
+          const int h = v >> 2, i = (v & 3) * 8;
+          uint4 o4;
+          o4.x = pack_bf16x2(__uint_as_float(o[h][i + 0]) * inv, __uint_as_float(o[h][i + 1]) * inv);
+          o4.y = pack_bf16x2(__uint_as_float(o[h][i + 2]) * inv, __uint_as_float(o[h][i + 3]) * inv);
+          o4.z = pack_bf16x2(__uint_as_float(o[h][i + 4]) * inv, __uint_as_float(o[h][i + 5]) * inv);
+          o4.w = pack_bf16x2(__uint_as_float(o[h][i + 6]) * inv, __uint_as_float(o[h][i + 7]) * inv);
+          dst[v] = o4;
         }
+        if (a.lse)
+          a.lse[grow] = (d_run > 0.f && m_run != -INFINITY) ? (m_run + __log2f(d_run)) * kLn2 : -INFINITY;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_ready[q]);
-    }
-
-    // ---------------------------------------------------------------- epilogue
-    uint32_t o[2][32];
-    bool have_o = false;
-    if (ok && n_kv > 0) {
-      const bool ready = mbar_wait(&bars->pv_done[q], (n_kv - 1) & 1, &bars->abort_word, a.err_flag);
-      have_o = __all_sync(0xffffffffu, ready);
-      if (have_o) {
-        tc_fence_after_sync();
-        tmem_ld32(o_taddr, o[0]);
-        tmem_ld32(o_taddr + 32, o[1]);
-        tmem_wait_ld();
-      }
-    }
-    if (!have_o) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[h][i] = 0u;
-    }
-    tc_fence_before_sync();
-    if (row_valid) {
-      const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
-      const long long grow = static_cast<long long>(q_start + tok) * a.Hq + head;
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const int h = v >> 2, i = (v & 3) * 8;
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[h][i + 0]) * inv, __uint_as_float(o[h][i + 1]) * inv);
-        w.y = pack_bf16x2(__uint_as_float(o[h][i + 2]) * inv, __uint_as_float(o[h][i + 3]) * inv);
-        w.z = pack_bf16x2(__uint_as_float(o[h][i + 4]) * inv, __uint_as_float(o[h][i + 5]) * inv);
-        w.w = pack_bf16x2(__uint_as_float(o[h][i + 6]) * inv, __uint_as_float(o[h][i + 7]) * inv);
-        dst[v] = w;
-      }
-      if (a.lse)
-        a.lse[grow] = (d_run > 0.f && m_run != -INFINITY) ? (m_run + __log2f(d_run)) * kLn2 : -INFINITY;
+      kv_it += w.n_kv;
+      it += w.n_kv;
     }
   }
 
@@ -450,13 +521,17 @@ cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
                                 const CUtensorMap& k_map, const CUtensorMap& v_map,
                                 cudaStream_t stream) {
   const int tok_per_cta = kQTiles * (kRows / a.group);
-  const int blocks = (a.max_q_len + tok_per_cta - 1) / tok_per_cta;
-  if (blocks > 65535) return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
+  const long long blocks = (a.max_q_len + tok_per_cta - 1) / tok_per_cta;
+  const long long n_tiles = blocks * a.B * a.Hkv;
+  if (n_tiles <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.Hkv, a.B, blocks);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, a);
+  e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(n_tiles < sms ? n_tiles : sms);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, a, n_tiles);
   return cudaGetLastError();
 }
 
