@@ -34,6 +34,38 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# dominant kernel, from the ncu captures summarised in profiles/.  A value holds
+# only for the kernel sources it was captured with (sha256 over the listed files);
+# after any change to them the roofline reports traffic = null.
+CSRC = "gqa_attention_sinks_gb300/csrc/"
+NCU_TRAFFIC = {
+    "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
+                                               "exp2_poly.cuh", "kernels.h")],
+                "sha256": "6bedbb68a87f0f366f7e2213178b6856755b3e13f53c41fa4ee19954512cbb44",
+                "bytes": 857580544},
+    "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
+               "sha256": "c669c8616bec8adc640508f7eb5160566e0a553b7a69e5cc5d2d4ccaf410cbc0",
+               "bytes": 583631872},
+}
+
+
+def sources_sha256(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kind):
+    e = NCU_TRAFFIC.get(kind)
+    if not e or not e["bytes"] or sources_sha256(e["files"]) != e["sha256"]:
+        return None
+    return e["bytes"]
+
+
 # ----------------------------------------------------------------- helpers
 def peaks():
     try:
@@ -257,7 +289,8 @@ def run_ours(args, ws, rank, local):
                        "bytes_per_step": nbytes},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(achieved / pk["hbm_gbs"], 4),
+                         "traffic": ncu_traffic("decode") if args.workload == "decode" else None,
                          "peak_source": pk_kind,
                          "kernel": "decode split kernel + LSE merge (one C-ABI call)"},
             "e2e": {"value": round(ws * nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
@@ -303,7 +336,7 @@ def run_ours(args, ws, rank, local):
                          "ms_per_step": round(pms, 4), "steps": psteps, "clocks": pclocks,
                          "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak,
                                       "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                                      "traffic": None, "peak_source": pk_kind}})
+                                      "traffic": ncu_traffic("prefill"), "peak_source": pk_kind}})
         except gas.AttnSinkError as e:
             part.update({"unavailable": str(e)})
         if result:

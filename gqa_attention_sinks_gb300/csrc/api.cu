@@ -110,7 +110,10 @@ DecodePlan plan_decode(int32_t B, int32_t Hkv, int32_t bt_stride, int32_t page_s
   }
   const long long max_units =
       (static_cast<long long>(bt_stride) * page_size + kUnitTokens - 1) / kUnitTokens;
-  int cu = 32;  // 512 keys = 128 KB of K+V per CTA for one KV head
+  // Start at 2048 keys (512 KB of K+V for one KV head) per CTA and halve while
+  // the grid would have fewer than 8 CTAs per SM; long chunks keep the fp32
+  // partials (and the merge) small.
+  int cu = 128;
   const long long target = 8LL * kGb300Sms;
   while (cu > 4 && static_cast<long long>(B) * Hkv * ((max_units + cu - 1) / cu) < target) cu /= 2;
   p.num_splits = 0;
