@@ -345,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(s_taddr + 32 * c, s[c]);
         tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_tie(s[c]);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free[q]);  // the MMA may now write the next S
@@ -353,16 +355,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool full = uok == 0xFFu && key_base + kKeys <= w.kv_len &&
                           (!a.causal || key_base + kKeys - 1 <= w.first_pos);
         if (!full) {
+          // Valid columns form a prefix [0, lim): keys below kv_len and, when
+          // causal, not after the row's position.  Skipped pages (rare) are
+          // cleared unit by unit.
+          int lim = w.kv_len - key_base;
+          if (a.causal) lim = min(lim, static_cast<int>(pos - key_base + 1));
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int col = 32 * c + i;
-              const int key = key_base + col;
-              const bool valid = key < w.kv_len && ((uok >> (col / kUnitTokens)) & 1u) &&
-                                 (!a.causal || key <= pos);
-              if (!valid) s[c][i] = __float_as_uint(-INFINITY);
-            }
+            for (int i = 0; i < 32; ++i)
+              if (32 * c + i >= lim) s[c][i] = __float_as_uint(-INFINITY);
+          if (uok != 0xFFu) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (!((uok >> ((32 * c + i) / kUnitTokens)) & 1u)) s[c][i] = __float_as_uint(-INFINITY);
+          }
         }
         // Row max: eight independent chains of 3-input max.
         float mx;
@@ -435,20 +444,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_unpack(f2_add(f2_add(ex2[0], ex2[1]), f2_add(ex2[2], ex2[3])), lo, hi);
           d_run += lo + hi;
         }
+        tmem_wait_st();
+        tmem_keep(p[0]);
+        tmem_keep(p[1]);
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           // (At j == 0 the first P*V of the work tile overwrites O instead.)
           uint32_t o[2][32];
           tmem_ld32(o_taddr, o[0]);
           tmem_ld32(o_taddr + 32, o[1]);
           tmem_wait_ld();
+          tmem_tie(o[0]);
+          tmem_tie(o[1]);
+          const uint64_t alpha2 = f2_pack(alpha, alpha);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[h][i] = __float_as_uint(__uint_as_float(o[h][i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              float lo, hi;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[h][i]), __uint_as_float(o[h][i + 1])), alpha2), lo, hi);
+              o[h][i] = __float_as_uint(lo);
+              o[h][i + 1] = __float_as_uint(hi);
+            }
           tmem_st32(o_taddr, o[0]);
           tmem_st32(o_taddr + 32, o[1]);
+          tmem_wait_st();
+          tmem_keep(o[0]);
+          tmem_keep(o[1]);
         }
-        tmem_wait_st();
         tc_fence_before_sync();
         if (q == 0 && !full) {
           // Keys this tile does not hold (past kv_len, or a skipped page) may sit
@@ -477,6 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(o_taddr, o[0]);
         tmem_ld32(o_taddr + 32, o[1]);
         tmem_wait_ld();
+        tmem_tie(o[0]);
+        tmem_tie(o[1]);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->o_free[q]);  // the next work tile may overwrite O
