@@ -22,7 +22,8 @@
 //              warpgroups take turns in the exponential loop.
 //   warp 8     TMA producer: per work tile the two Q tiles (double-buffered),
 //              then per 128-key tile eight 16-row page slices of K and of V
-//              into a 3-stage ring.  It runs ahead across work tiles.
+//              into a 4-stage ring.  It runs ahead across work tiles and reads
+//              the block-table entries one tile ahead.
 //   warps 9-10 one MMA-issuing warp per Q tile (warp 9 also owns TMEM).
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,320), O1 [320,384),
 // P0 [384,448), P1 [448,512) (P as packed bf16 pairs).
@@ -43,7 +44,7 @@ namespace {
 constexpr int kRows = 128;
 constexpr int kQTiles = 2;
 constexpr int kKeys = 128;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kQBufs = 2;
 constexpr int kUnitsPerTile = kKeys / kUnitTokens;            // 8
 constexpr int kUnitBytes = kUnitTokens * kHeadDim * 2;       // 2 KB
@@ -198,7 +199,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++qw;
       const int32_t* bt_row = a.block_table + static_cast<long long>(w.b) * a.bt_stride;
+      // lane u < 8 holds the block-table entry of unit u of a tile (-1 past kv_len)
+      auto entry_of = [&](int jj) -> int {
+        const int key0 = (jj * kUnitsPerTile + lane) * kUnitTokens;
+        return (lane < kUnitsPerTile && jj < w.n_kv && key0 < w.kv_len) ? bt_row[key0 / a.page_size] : -1;
+      };
+      int next_phys = entry_of(0);
       for (int j = 0; j < w.n_kv; ++j, ++kv_it) {
+        const int cur_phys = next_phys;
+        next_phys = entry_of(j + 1);
         const int st = kv_it % kStages;
         if (kv_it >= kStages) {
           const bool ready = mbar_wait(&bars->kv_empty[st], ((kv_it / kStages) + 1) & 1, abort_word,
@@ -211,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < kUnitsPerTile) {
           const int key0 = (j * kUnitsPerTile + lane) * kUnitTokens;
           if (key0 < w.kv_len) {
-            const int phys = bt_row[key0 / a.page_size];
+            const int phys = cur_phys;
             unit_ok = phys >= 0 && phys < a.num_pages;
             bad = !unit_ok;
             row = phys * a.page_size + key0 % a.page_size;
@@ -354,6 +363,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key_base = j * kKeys;
         const bool full = uok == 0xFFu && key_base + kKeys <= w.kv_len &&
                           (!a.causal || key_base + kKeys - 1 <= w.first_pos);
+        if (uok != 0xFFu || key_base + kKeys > w.kv_len) {
+          // Keys this tile does not hold (past kv_len, or a skipped page) may sit
+          // over stale shared memory: their P is 0, but 0 * NaN is NaN, so thread
+          // r clears V row r.  The stage has landed (kv_full above) and this
+          // warpgroup's P*V is issued only after its p_ready below; each Q tile's
+          // P*V waits only for its own warpgroup, so both clear the rows (the same
+          // zeros).
+          const bool held = key_base + r < w.kv_len && ((uok >> (r / kUnitTokens)) & 1u);
+          if (!held) {
+            uint4* vrow = reinterpret_cast<uint4*>(base + kOffKV + st * kStageBytes + kTileBytes + r * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+          }
+        }
         if (!full) {
           // Valid columns form a prefix [0, lim): keys below kv_len and, when
           // causal, not after the row's position.  Skipped pages (rare) are
@@ -472,18 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_keep(o[1]);
         }
         tc_fence_before_sync();
-        if (q == 0 && !full) {
-          // Keys this tile does not hold (past kv_len, or a skipped page) may sit
-          // over stale shared memory: their P is 0, but 0 * NaN is NaN, so clear V.
-          const int col = r;
-          const bool held = key_base + col < w.kv_len && ((uok >> (col / kUnitTokens)) & 1u);
-          if (!held) {
-            uint4* vrow = reinterpret_cast<uint4*>(base + kOffKV + st * kStageBytes + kTileBytes + col * 128);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();
-          }
-        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_ready[q]);
       }
