@@ -20,11 +20,16 @@
 //              max/exp2/sum run in registers, P (bf16) goes back into TMEM in
 //              its own columns and feeds P*V as the A operand.  The two
 //              warpgroups take turns in the exponential loop.
-//   warp 8     TMA producer: per work tile the two Q tiles (double-buffered),
-//              then per 128-key tile eight 16-row page slices of K and of V
-//              into a 4-stage ring.  It runs ahead across work tiles and reads
-//              the block-table entries one tile ahead.
+//   warp 8     TMA producer of Q and K: per work tile the two Q tiles
+//              (double-buffered), then per 128-key tile eight 16-row page
+//              slices of K into a 4-stage ring.  It runs ahead across work
+//              tiles and reads the block-table entries one tile ahead.
 //   warps 9-10 one MMA-issuing warp per Q tile (warp 9 also owns TMEM).
+//   warp 11    TMA producer of V, in step with warp 8.  A 2 KB page slice
+//              occupies the SM's TMA unit for about 90 clocks, so the sixteen
+//              slices of a tile take as long as the tile's MMAs; two issuing
+//              warps on different SMSPs keep the unit fed while each one
+//              computes addresses and waits on barriers.
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,320), O1 [320,384),
 // P0 [384,448), P1 [448,512) (P as packed bf16 pairs).
 //
@@ -52,10 +57,11 @@ constexpr int kTileBytes = kRows * kHeadDim * 2;             // 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;                  // K then V
 constexpr int kQBufBytes = kQTiles * kTileBytes;
 constexpr int kSoftmaxWarps = 4 * kQTiles;
-// One producer warp, then one MMA-issuing warp per Q tile (the first of them
-// also allocates TMEM).
+// The Q/K producer warp, one MMA-issuing warp per Q tile (the first of them
+// also allocates TMEM), then the V producer warp.
 constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kQTiles);
+constexpr int kProducerWarpV = kMmaWarp + kQTiles;
+constexpr int kThreads = 32 * (kProducerWarpV + 1);
 constexpr uint32_t kTmemCols = 256 * kQTiles;  // S, O and P of every Q tile
 __device__ __forceinline__ uint32_t col_s(int q) { return static_cast<uint32_t>(q) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int q) { return 128u * kQTiles + static_cast<uint32_t>(q) * 64u; }
@@ -63,7 +69,12 @@ __device__ __forceinline__ uint32_t col_p(int q) { return 192u * kQTiles + stati
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kQBufs * kQBufBytes;
 constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
+// Per-sequence lengths and per-head sinks are copied to shared memory when
+// they fit, so that decoding a work tile costs no global-memory round trip.
+constexpr int kMetaSeqs = 1024, kMetaHeads = 256;
+constexpr int kOffMeta = kOffBar + 256;
+constexpr int kMetaBytes = ((2 * kMetaSeqs + 1 + kMetaHeads) * 4 + 255) / 256 * 256;
+constexpr int kSmemBytes = kOffMeta + kMetaBytes + 1024;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
@@ -93,6 +104,14 @@ struct alignas(8) Bars {
   int abort_word;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+
+// Where the per-sequence lengths and the sinks are read from.
+struct Meta {
+  const int32_t* cu_seqlens_q;
+  const int32_t* kv_lens;
+  const float* sinks;
+};
 
 // A work tile, derived identically by every role from its linear index.
 struct WorkTile {
@@ -100,19 +119,19 @@ struct WorkTile {
   long long first_pos;  // absolute position of the tile's first query
 };
 
-__device__ __forceinline__ bool decode_tile(const PrefillArgs& a, long long t, int tok_per_cta,
-                                            WorkTile& w) {
+__device__ __forceinline__ bool decode_tile(const PrefillArgs& a, const Meta& m, long long t,
+                                            int tok_per_cta, WorkTile& w) {
   const long long heads = static_cast<long long>(a.B) * a.Hkv;
   const int r = static_cast<int>(t / heads);  // 0: last query block of each sequence
   const int rem = static_cast<int>(t % heads);
   w.b = rem / a.Hkv;
   w.g = rem % a.Hkv;
-  w.q_start = a.cu_seqlens_q[w.b];
-  w.q_len = a.cu_seqlens_q[w.b + 1] - w.q_start;
+  w.q_start = m.cu_seqlens_q[w.b];
+  w.q_len = m.cu_seqlens_q[w.b + 1] - w.q_start;
   const int n_blocks = w.q_len > 0 ? (w.q_len + tok_per_cta - 1) / tok_per_cta : 0;
   if (r >= n_blocks) return false;
   w.tok0 = (n_blocks - 1 - r) * tok_per_cta;
-  w.kv_raw = max(0, a.kv_lens[w.b]);
+  w.kv_raw = max(0, m.kv_lens[w.b]);
   w.kv_len = min(w.kv_raw, a.bt_stride * a.page_size);  // keys beyond the table row are not read
   w.first_pos = static_cast<long long>(w.kv_len) - w.q_len + w.tok0;
   const long long last_pos =
@@ -145,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_empty[i], kQTiles);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_full[s], 2);   // the K and the V producer
       mbar_init(&bars->kv_empty[s], kQTiles);  // released by every Q tile's P*V
     }
     for (int q = 0; q < kQTiles; ++q) {
@@ -164,17 +183,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  Meta meta{a.cu_seqlens_q, a.kv_lens, a.sinks};
+  if (a.B <= kMetaSeqs && a.Hq <= kMetaHeads) {
+    int32_t* cu_s = reinterpret_cast<int32_t*>(base + kOffMeta);
+    int32_t* kvl_s = cu_s + kMetaSeqs + 1;
+    float* sinks_s = reinterpret_cast<float*>(kvl_s + kMetaSeqs);
+    for (int i = threadIdx.x; i <= a.B; i += kThreads) cu_s[i] = a.cu_seqlens_q[i];
+    for (int i = threadIdx.x; i < a.B; i += kThreads) kvl_s[i] = a.kv_lens[i];
+    for (int i = threadIdx.x; i < a.Hq; i += kThreads) sinks_s[i] = a.sinks[i];
+    meta = Meta{cu_s, kvl_s, sinks_s};
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp || warp == kProducerWarpV) {
     // ---------------------------------------------------------------- TMA
+    const bool is_k = warp == kProducerWarp;  // else the V producer
+    const CUtensorMap* kv_map = is_k ? &k_map : &v_map;
+    const int kv_off = is_k ? 0 : kTileBytes;
     if (lane == 0) {
-      tma_prefetch_map(&q_map);
-      tma_prefetch_map(&k_map);
-      tma_prefetch_map(&v_map);
+      if (is_k) tma_prefetch_map(&q_map);
+      tma_prefetch_map(kv_map);
     }
     const uint64_t once = l2_policy_evict_first();   // each Q tile is read by one CTA
     const uint64_t reuse = l2_policy_evict_last();   // K/V tiles serve every later query block
@@ -182,22 +213,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       WorkTile w;
-      if (!decode_tile(a, t, tok_per_cta, w)) continue;
-      if (w.kv_len < w.kv_raw && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
+      if (!decode_tile(a, meta, t, tok_per_cta, w)) continue;
+      if (is_k && w.kv_len < w.kv_raw && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
       if (w.n_kv == 0) continue;
-      const int qb = qw % kQBufs;
-      if (qw >= kQBufs) {
-        const bool ready = mbar_wait(&bars->q_empty[qb], ((qw / kQBufs) + 1) & 1, abort_word, a.err_flag);
-        ok = __all_sync(0xffffffffu, ready);
-        if (!ok) break;
+      if (is_k) {
+        const int qb = qw % kQBufs;
+        if (qw >= kQBufs) {
+          const bool ready = mbar_wait(&bars->q_empty[qb], ((qw / kQBufs) + 1) & 1, abort_word, a.err_flag);
+          ok = __all_sync(0xffffffffu, ready);
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->q_full[qb], kQBufBytes);
+          for (int q = 0; q < kQTiles; ++q)
+            tma_load_3d_hint(base + kOffQ + qb * kQBufBytes + q * kTileBytes, &q_map, &bars->q_full[qb],
+                             0, w.g * a.group, w.q_start + w.tok0 + q * tok_per_tile, once);
+        }
+        ++qw;
       }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full[qb], kQBufBytes);
-        for (int q = 0; q < kQTiles; ++q)
-          tma_load_3d_hint(base + kOffQ + qb * kQBufBytes + q * kTileBytes, &q_map, &bars->q_full[qb],
-                           0, w.g * a.group, w.q_start + w.tok0 + q * tok_per_tile, once);
-      }
-      ++qw;
       const int32_t* bt_row = a.block_table + static_cast<long long>(w.b) * a.bt_stride;
       // lane u < 8 holds the block-table entry of unit u of a tile (-1 past kv_len)
       auto entry_of = [&](int jj) -> int {
@@ -226,94 +259,105 @@ __global__ void __launch_bounds__(kThreads, 1)
             row = phys * a.page_size + key0 % a.page_size;
           }
         }
+        // Both producers derive the same mask from the same table entries.
         const uint32_t ok_mask = __ballot_sync(0xffffffffu, unit_ok);
-        if (__ballot_sync(0xffffffffu, bad) && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
+        if (is_k && __ballot_sync(0xffffffffu, bad) && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
         if (lane == 0) {
-          bars->unit_ok[st] = ok_mask;  // published by the arrive below (release)
-          mbar_arrive_expect_tx(&bars->kv_full[st], __popc(ok_mask) * 2 * kUnitBytes);
+          if (is_k) bars->unit_ok[st] = ok_mask;  // published by the arrive below (release)
+          mbar_arrive_expect_tx(&bars->kv_full[st], __popc(ok_mask) * kUnitBytes);
         }
         __syncwarp();
-        if (unit_ok) {
-          uint8_t* stage = base + kOffKV + st * kStageBytes;
-          tma_load_2d_hint(stage + lane * kUnitBytes, &k_map, &bars->kv_full[st], w.g * kHeadDim,
-                           row, reuse);
-          tma_load_2d_hint(stage + kTileBytes + lane * kUnitBytes, &v_map, &bars->kv_full[st],
-                           w.g * kHeadDim, row, reuse);
-        }
+        if (unit_ok)
+          tma_load_2d_hint(base + kOffKV + st * kStageBytes + kv_off + lane * kUnitBytes, kv_map,
+                           &bars->kv_full[st], w.g * kHeadDim, row, reuse);
       }
     }
     if (lane == 0) {  // every issued copy lands before the CTA leaves
-      for (int i = max(0, qw - kQBufs); i < qw; ++i)
+      for (int i = max(0, qw - kQBufs); is_k && i < qw; ++i)
         mbar_wait_drain(&bars->q_full[i % kQBufs], (i / kQBufs) & 1);
       for (int i = max(0, kv_it - kStages); i < kv_it; ++i)
         mbar_wait_drain(&bars->kv_full[i % kStages], (i / kStages) & 1);
     }
-  } else if (warp >= kMmaWarp) {
+  } else if (warp >= kMmaWarp && warp < kMmaWarp + kQTiles) {
     // ---------------------------------------------------------------- MMA
     // Warp kMmaWarp + q issues every MMA of Q tile q, so the two tiles'
-    // pipelines never wait on each other.
+    // pipelines never wait on each other.  The whole warp runs the loop (its
+    // descriptors stay warp-uniform); one elected lane issues.  A descriptor
+    // differs from the stage-0 one only in its start-address field, so each
+    // MMA's operands cost one add.
     const int q = warp - kMmaWarp;
-    if (lane == 0) {
-      auto issue_s = [&](uint32_t q_addr, uint32_t k_addr) {
+    const uint64_t q_desc0 = smem_desc_sw128(smem_addr(base + kOffQ + q * kTileBytes), 16, 1024);
+    const uint64_t k_desc0 = smem_desc_sw128(smem_addr(base + kOffKV), 16, 1024);
+    const uint64_t v_desc0 = smem_desc_sw128(smem_addr(base + kOffKV + kTileBytes), 8192, 1024);
+    constexpr uint32_t kStageDesc = kStageBytes >> 4, kQBufDesc = kQBufBytes >> 4;
+    const uint32_t tmem_s = tmem + col_s(q), tmem_o = tmem + col_o(q), tmem_p = tmem + col_p(q);
+    const bool leader = elect_one();
+    auto issue_s = [&](int qb, int st) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          umma_ss(tmem + col_s(q), smem_desc_sw128(q_addr + kk * 32, 16, 1024),
-                  smem_desc_sw128(k_addr + kk * 32, 16, 1024), kIdescS, kk > 0);
-      };
-      auto issue_pv = [&](int st, bool acc) {
-        const uint32_t v_addr = smem_addr(base + kOffKV + st * kStageBytes + kTileBytes);
+          umma_ss(tmem_s, q_desc0 + qb * kQBufDesc + kk * 2, k_desc0 + st * kStageDesc + kk * 2, kIdescS,
+                  kk > 0);
+        umma_commit(&bars->s_full[q]);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int st, bool acc) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma_ts(tmem + col_o(q), tmem + col_p(q) + kk * 8,
-                  smem_desc_sw128(v_addr + kk * 2048, 8192, 1024), kIdescPV, acc || kk > 0);
-      };
-      auto kv_addr = [&](int it) { return smem_addr(base + kOffKV + (it % kStages) * kStageBytes); };
-      int qw = 0, kv_it = 0, it = 0, ow = 0;
-      bool ok = true;
-      for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        WorkTile w;
-        if (!decode_tile(a, t, tok_per_cta, w) || w.n_kv == 0) continue;
-        const int qb = qw % kQBufs;
-        const uint32_t q_addr = smem_addr(base + kOffQ + qb * kQBufBytes + q * kTileBytes);
-        // Q loaded, the first K/V tile in, and the previous S read out of TMEM.
-        ok = mbar_wait(&bars->q_full[qb], (qw / kQBufs) & 1, abort_word, a.err_flag) &&
-             mbar_wait(&bars->kv_full[kv_it % kStages], (kv_it / kStages) & 1, abort_word, a.err_flag) &&
-             (it == 0 || mbar_wait(&bars->s_free[q], (it - 1) & 1, abort_word, a.err_flag));
-        if (!ok) break;
-        tc_fence_after_sync();
-        issue_s(q_addr, kv_addr(kv_it));
-        umma_commit(&bars->s_full[q]);
-        for (int j = 0; j < w.n_kv; ++j) {
-          const int cur = kv_it + j, u = it + j;
-          if (j + 1 < w.n_kv) {
-            ok = mbar_wait(&bars->kv_full[(cur + 1) % kStages], ((cur + 1) / kStages) & 1, abort_word,
-                           a.err_flag) &&
-                 mbar_wait(&bars->s_free[q], u & 1, abort_word, a.err_flag);
-            if (!ok) break;
-            tc_fence_after_sync();
-            issue_s(q_addr, kv_addr(cur + 1));
-            umma_commit(&bars->s_full[q]);
-          }
-          // The first P*V of a work tile overwrites O: the previous tile's O must
-          // have been read out by then.
-          ok = mbar_wait(&bars->p_ready[q], u & 1, abort_word, a.err_flag) &&
-               (j > 0 || ow == 0 || mbar_wait(&bars->o_free[q], (ow - 1) & 1, abort_word, a.err_flag));
+          umma_ts(tmem_o, tmem_p + kk * 8, v_desc0 + st * kStageDesc + kk * 128, kIdescPV, acc || kk > 0);
+        umma_commit(&bars->pv_done[q]);
+        umma_commit(&bars->kv_empty[st]);
+      }
+      __syncwarp();
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_word, a.err_flag));
+    };
+    int qw = 0, kv_it = 0, it = 0, ow = 0;
+    bool ok = true;
+    for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      WorkTile w;
+      if (!decode_tile(a, meta, t, tok_per_cta, w) || w.n_kv == 0) continue;
+      const int qb = qw % kQBufs;
+      // Q loaded, the first K/V tile in, and the previous S read out of TMEM.
+      ok = wait_all(&bars->q_full[qb], (qw / kQBufs) & 1) &&
+           wait_all(&bars->kv_full[kv_it % kStages], (kv_it / kStages) & 1) &&
+           (it == 0 || wait_all(&bars->s_free[q], (it - 1) & 1));
+      if (!ok) break;
+      tc_fence_after_sync();
+      issue_s(qb, kv_it % kStages);
+      for (int j = 0; j < w.n_kv; ++j) {
+        const int cur = kv_it + j, u = it + j;
+        if (j + 1 < w.n_kv) {
+          ok = wait_all(&bars->kv_full[(cur + 1) % kStages], ((cur + 1) / kStages) & 1) &&
+               wait_all(&bars->s_free[q], u & 1);
           if (!ok) break;
           tc_fence_after_sync();
-          issue_pv(cur % kStages, j > 0);
-          umma_commit(&bars->pv_done[q]);
-          umma_commit(&bars->kv_empty[cur % kStages]);
+          issue_s(qb, (cur + 1) % kStages);
         }
+        // The first P*V of a work tile overwrites O: the previous tile's O must
+        // have been read out by then.
+        ok = wait_all(&bars->p_ready[q], u & 1) &&
+             (j > 0 || ow == 0 || wait_all(&bars->o_free[q], (ow - 1) & 1));
         if (!ok) break;
-        umma_commit(&bars->q_empty[qb]);
-        ++qw;
-        kv_it += w.n_kv;
-        it += w.n_kv;
-        ++ow;
+        tc_fence_after_sync();
+        issue_pv(cur % kStages, j > 0);
       }
+      if (!ok) break;
+      if (leader) umma_commit(&bars->q_empty[qb]);
+      __syncwarp();
+      ++qw;
+      kv_it += w.n_kv;
+      it += w.n_kv;
+      ++ow;
+    }
+    if (leader) {
       umma_commit(&bars->mma_done);
       mbar_wait_drain(&bars->mma_done, 0);  // no MMA may still write TMEM at dealloc
     }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax
     const int q = warp >> 2;
@@ -332,12 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       WorkTile w;
-      if (!decode_tile(a, t, tok_per_cta, w)) continue;
+      if (!decode_tile(a, meta, t, tok_per_cta, w)) continue;
       const int tok = w.tok0 + q * tok_per_tile + r / a.group;
       const int head = w.g * a.group + r % a.group;
       const bool row_valid = tok < w.q_len;
       const long long pos = static_cast<long long>(w.kv_len) - w.q_len + tok;
-      float m_run = a.sinks[head] * kLog2e;  // the sink is the initial running max ...
+      float m_run = meta.sinks[head] * kLog2e;  // the sink is the initial running max ...
       float d_run = 1.f;                     // ... with running sum e^0 = 1
       for (int j = 0; j < w.n_kv; ++j) {
         const int cur = kv_it + j, u = it + j;
