@@ -42,11 +42,11 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "6bedbb68a87f0f366f7e2213178b6856755b3e13f53c41fa4ee19954512cbb44",
-                "bytes": 857580544},
+                "sha256": "cc177fbe2bed010e41c53390b21f85b0a423c3957b6eea3a7669081facc3673b",
+                "bytes": 810618368},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
-               "sha256": "c669c8616bec8adc640508f7eb5160566e0a553b7a69e5cc5d2d4ccaf410cbc0",
-               "bytes": 583631872},
+               "sha256": "a22883ce5ebe4619948a44cd84545bc5aec03c505024729e702058f38d66db86",
+               "bytes": 583284480},
 }
 
 

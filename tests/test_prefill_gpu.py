@@ -47,6 +47,22 @@ def test_prefill_with_prefix(cuda_lib):
     _check_all(cuda_lib, _batch(22, [64, 100, 5, 130], prefix=[0, 300, 17, 1000]), "prefix")
 
 
+def test_prefill_many_sequences_global_metadata(cuda_lib):
+    """1100 short sequences: more than the kernel keeps in shared memory, so work
+    tiles are decoded from the global length arrays (and a few with long prefixes)."""
+    rng = np.random.default_rng(31)
+    q_lens = rng.integers(1, 6, 1100)
+    prefix = rng.integers(0, 40, 1100)
+    prefix[::97] = 300
+    _check_all(cuda_lib, _batch(31, q_lens, prefix=prefix, Hq=16, Hkv=2), "1100 sequences")
+
+
+def test_prefill_many_heads_global_sinks(cuda_lib):
+    """Hq = 288 query heads (group 16 over 18 KV heads): more sinks than the
+    kernel keeps in shared memory."""
+    _check_all(cuda_lib, _batch(32, [40, 9], prefix=[0, 20], Hq=288, Hkv=18), "288 heads")
+
+
 def test_prefill_non_causal(cuda_lib):
     batch = _batch(23, [50, 129], prefix=[10, 60], causal=False)
     _check_all(cuda_lib, batch, "non-causal")
