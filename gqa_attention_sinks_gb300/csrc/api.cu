@@ -67,6 +67,24 @@ bool make_map_q(CUtensorMap* map, const void* base, uint64_t total_q, uint64_t H
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D bf16 tensor map over a paged NHD cache [num_pages, page_size, Hkv, 64]
+// ordered (dim, token in page, head, page), box {64, 16, kHeadsPerCta, 1}: one
+// copy brings a 16-token slice of kHeadsPerCta heads, each head's 16 rows
+// contiguous (2 KB) in shared memory.  The head stride (128 B) is below the
+// token stride; TMA takes each dimension's stride as given.
+bool make_map_paged_heads(CUtensorMap* map, const void* base, uint64_t num_pages,
+                          uint64_t page_size, uint64_t Hkv) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {64, page_size, Hkv, num_pages};
+  cuuint64_t strides[3] = {Hkv * 64 * 2, 64 * 2, page_size * Hkv * 64 * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kUnitTokens), static_cast<cuuint32_t>(kHeadsPerCta), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 attn_sink_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return ATTN_SINK_OK;
   if (e == cudaErrorNotSupported) return ATTN_SINK_ERR_UNSUPPORTED;
@@ -110,12 +128,13 @@ DecodePlan plan_decode(int32_t B, int32_t Hkv, int32_t bt_stride, int32_t page_s
   }
   const long long max_units =
       (static_cast<long long>(bt_stride) * page_size + kUnitTokens - 1) / kUnitTokens;
-  // Start at 2048 keys (512 KB of K+V for one KV head) per CTA and halve while
-  // the grid would have fewer than 8 CTAs per SM; long chunks keep the fp32
-  // partials (and the merge) small.
+  // A CTA covers kHeadsPerCta KV heads.  Start at 2048 keys per CTA and halve
+  // while the grid would have fewer than 8 CTAs per SM; long chunks keep the
+  // fp32 partials (and the merge) small.
+  const long long groups = (Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
   int cu = 128;
   const long long target = 8LL * kGb300Sms;
-  while (cu > 4 && static_cast<long long>(B) * Hkv * ((max_units + cu - 1) / cu) < target) cu /= 2;
+  while (cu > 4 && static_cast<long long>(B) * groups * ((max_units + cu - 1) / cu) < target) cu /= 2;
   p.num_splits = 0;
   p.chunk_units = cu;
   p.max_chunks = static_cast<int>(std::max(1LL, (max_units + cu - 1) / cu));
@@ -227,9 +246,10 @@ ATTN_SINK_API attn_sink_status attn_sink_decode(
     return ATTN_SINK_ERR_WORKSPACE;
 
   CUtensorMap k_map, v_map;
-  const uint64_t rows = static_cast<uint64_t>(num_pages) * page_size;
-  if (!make_map_2d(&k_map, k_cache, static_cast<uint64_t>(Hkv) * kHeadDim, rows, kUnitTokens) ||
-      !make_map_2d(&v_map, v_cache, static_cast<uint64_t>(Hkv) * kHeadDim, rows, kUnitTokens))
+  if (!make_map_paged_heads(&k_map, k_cache, static_cast<uint64_t>(num_pages),
+                            static_cast<uint64_t>(page_size), static_cast<uint64_t>(Hkv)) ||
+      !make_map_paged_heads(&v_map, v_cache, static_cast<uint64_t>(num_pages),
+                            static_cast<uint64_t>(page_size), static_cast<uint64_t>(Hkv)))
     return ATTN_SINK_ERR_CUDA;
 
   DecodeArgs a{};

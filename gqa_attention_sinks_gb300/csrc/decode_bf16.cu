@@ -1,23 +1,27 @@
 // Split-KV paged decode for bf16 sink attention on sm_103a.
 //
-// One CTA owns (chunk c, KV head g, sequence b) and all G query heads of that
-// group, so every K/V byte of the chunk is read from HBM exactly once.
+// One CTA owns (chunk c, a group of kHeadsPerCta KV heads, sequence b) and all
+// G query heads of each of those KV heads, so every K/V byte of the chunk is
+// read from HBM exactly once.
 // "GPT-OSS pada Hari ke-0", section "Atensi Sink": attention is parallelised
 // over heads and along the KV length; the online softmax starts its running
 // maximum at the head's sink value with running sum 1, and only the first
 // chunk of a split may do so.
 //
 // Warp roles (160 threads):
-//   warp 4      producer: reads the block table and issues one TMA box per
-//               16-key unit (16 rows x 128 B of one KV head) for K and V into a
-//               4-stage shared-memory ring guarded by mbarriers.
-//   warps 0..3  consumers: warp w takes unit w of each stage.  Scores for the
-//               G packed heads (M = 16 rows) come from mma.sync m16n8k16 bf16
+//   warp 4      producer: reads the block table (32 units ahead) and per
+//               16-key unit issues one TMA box for K and one for V that cover
+//               the unit's 16 rows of all kHeadsPerCta heads (8 KB each; a 4-D
+//               tensor map over (dim, token in page, head, page)), into a
+//               4-stage shared-memory ring guarded by mbarriers.  A 2 KB box
+//               per head and unit occupies the SM's TMA unit about as long as
+//               an 8 KB one, so this keeps TMA far from the HBM rate.
+//   warps 0..3  consumers: warp w owns KV head g0 + w.  Scores for the G packed
+//               query heads (M = 16 rows) come from mma.sync m16n8k16 bf16
 //               with fp32 accumulation, the online softmax runs in registers,
 //               and P*V reuses the score fragments as the A operand.
-// The four warps' states are merged through shared memory at the end and the
-// CTA writes either the final output (the sequence has one chunk) or an fp32
-// partial (o, lse) that the merge kernel combines.
+// Each warp writes either its heads' final output (the sequence has one
+// chunk) or an fp32 partial (o, lse) that the merge kernel combines.
 //
 // The kernel is HBM-bound: per key and KV head it moves 256 B and does
 // 2*G*64 MACs, which the tensor-core path hides completely.
@@ -28,11 +32,11 @@ namespace attn_sink {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kUnitsPerStage = kConsumerWarps;
 constexpr int kStages = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kUnitBytes = kUnitTokens * kHeadDim * 2;              // 2048
-constexpr int kStageBytes = 2 * kUnitsPerStage * kUnitBytes;         // 16 KB (K then V)
+constexpr int kUnitBytes = kUnitTokens * kHeadDim * 2;              // 2048: one head, one unit
+constexpr int kHalfBytes = kHeadsPerCta * kUnitBytes;               // 8 KB: one box
+constexpr int kStageBytes = 2 * kHalfBytes;                          // 16 KB (K then V)
 constexpr int kRingBytes = kStages * kStageBytes;                    // 64 KB
 constexpr int kSmemBytes = kRingBytes + 1024 /*align slack*/ + 128 /*barriers*/;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -41,9 +45,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct alignas(8) Barriers {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint32_t unit_ok[kStages];
+  uint32_t unit_ok[kStages];  // the stage's unit was loaded (its page index is valid)
   int abort_word;
 };
+static_assert(kConsumerWarps == kHeadsPerCta, "one consumer warp per KV head of the CTA");
 
 __device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
                                         uint32_t addr) {
@@ -199,13 +204,13 @@ __global__ void __launch_bounds__(kThreads)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Barriers* bars = reinterpret_cast<Barriers*>(ring + kRingBytes);
 
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int c = blockIdx.x, g0 = blockIdx.y * kHeadsPerCta, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- chunk bounds in 16-key units (keys beyond the table row are not read)
   const int kv_raw = a.kv_lens[b] > 0 ? a.kv_lens[b] : 0;
   const int kv_len = min(kv_raw, a.bt_stride * a.page_size);
-  if (kv_len < kv_raw && threadIdx.x == 0 && c == 0 && g == 0 && a.err_flag)
+  if (kv_len < kv_raw && threadIdx.x == 0 && c == 0 && g0 == 0 && a.err_flag)
     atomicOr(a.err_flag, kFlagBadPage);
   const int n_units_seq = (kv_len + kUnitTokens - 1) / kUnitTokens;
   int u0, u1, n_chunks;
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kThreads)
     u1 = min(u0 + a.chunk_units, n_units_seq);
   }
   if (u1 < u0) u1 = u0;
-  const int n_iters = (u1 - u0 + kUnitsPerStage - 1) / kUnitsPerStage;
+  const int n_iters = u1 - u0;  // one unit per stage
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -243,39 +248,49 @@ __global__ void __launch_bounds__(kThreads)
     }
     const uint64_t policy = l2_policy_evict_first();
     const int32_t* bt_row = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    const int units_per_page = a.page_size / kUnitTokens;
+    // Lane l holds the page and in-page row of unit u0 + 32k + l for the
+    // current window of 32 units; the next window is read while this one is
+    // used.
+    auto fetch = [&](int base, int& phys, int& tok) {
+      const int u = u0 + base + lane;
+      phys = -1;
+      tok = 0;
+      if (u < u1) {
+        phys = bt_row[u / units_per_page];
+        tok = (u % units_per_page) * kUnitTokens;
+      }
+    };
+    int cur_phys, cur_tok, nxt_phys, nxt_tok;
+    fetch(0, cur_phys, cur_tok);
+    fetch(32, nxt_phys, nxt_tok);
     int issued = 0;
     for (int it = 0; it < n_iters; ++it) {
+      if (it > 0 && (it & 31) == 0) {
+        cur_phys = nxt_phys;
+        cur_tok = nxt_tok;
+        fetch(it + 32, nxt_phys, nxt_tok);
+      }
       const int stage = it % kStages;
       if (it >= kStages) {
         const bool ready = mbar_wait(&bars->empty[stage], ((it / kStages) + 1) & 1,
                                      &bars->abort_word, a.err_flag);
         if (!__all_sync(0xffffffffu, ready)) break;
       }
-      const int u = u0 + it * kUnitsPerStage + lane;
-      bool ok = false, bad = false;
-      int row = 0;
-      if (lane < kUnitsPerStage && u < u1) {
-        const int key0 = u * kUnitTokens;
-        const int phys = bt_row[key0 / a.page_size];
-        ok = phys >= 0 && phys < a.num_pages;
-        bad = !ok;
-        row = phys * a.page_size + (key0 % a.page_size);
-      }
-      const uint32_t ok_mask = __ballot_sync(0xffffffffu, ok);
-      if (__ballot_sync(0xffffffffu, bad) && lane == 0 && a.err_flag)
-        atomicOr(a.err_flag, kFlagBadPage);
+      const int phys = __shfl_sync(0xffffffffu, cur_phys, it & 31);
+      const int tok = __shfl_sync(0xffffffffu, cur_tok, it & 31);
+      const bool ok = phys >= 0 && phys < a.num_pages;
       if (lane == 0) {
-        bars->unit_ok[stage] = ok_mask;
-        mbar_arrive_expect_tx(&bars->full[stage], __popc(ok_mask) * 2 * kUnitBytes);
+        if (!ok && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
+        bars->unit_ok[stage] = ok ? 1u : 0u;
+        mbar_arrive_expect_tx(&bars->full[stage], ok ? kStageBytes : 0);
+        if (ok) {
+          uint8_t* st = ring + stage * kStageBytes;
+          tma_load_4d_hint(st, &k_map, &bars->full[stage], 0, tok, g0, phys, policy);
+          tma_load_4d_hint(st + kHalfBytes, &v_map, &bars->full[stage], 0, tok, g0, phys, policy);
+        }
       }
       __syncwarp();
-      if (ok) {
-        uint8_t* st = ring + stage * kStageBytes;
-        tma_load_2d_hint(st + lane * kUnitBytes, &k_map, &bars->full[stage], g * kHeadDim, row,
-                         policy);
-        tma_load_2d_hint(st + (kUnitsPerStage + lane) * kUnitBytes, &v_map, &bars->full[stage],
-                         g * kHeadDim, row, policy);
-      }
       issued = it + 1;
     }
     // Drain: every issued load lands before the CTA's shared memory goes away.
@@ -287,6 +302,8 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // -------------------------------------------------------------- consumers
+  const int g = g0 + warp;            // this warp's KV head
+  const bool head_ok = g < a.Hkv;
   const int r0 = lane >> 2, r1 = r0 + 8;
   const int head0 = g * a.group;
   uint32_t qa[4][4];
@@ -294,13 +311,14 @@ __global__ void __launch_bounds__(kThreads)
     const __nv_bfloat16* qb =
         reinterpret_cast<const __nv_bfloat16*>(a.q) + (static_cast<long long>(b) * a.Hq + head0) * kHeadDim;
     const int col = 2 * (lane & 3);
+    const bool ok0 = head_ok && r0 < a.group, ok1 = head_ok && r1 < a.group;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       const int d = 16 * ks + col;
-      qa[ks][0] = r0 < a.group ? *reinterpret_cast<const uint32_t*>(qb + r0 * kHeadDim + d) : 0u;
-      qa[ks][1] = r1 < a.group ? *reinterpret_cast<const uint32_t*>(qb + r1 * kHeadDim + d) : 0u;
-      qa[ks][2] = r0 < a.group ? *reinterpret_cast<const uint32_t*>(qb + r0 * kHeadDim + d + 8) : 0u;
-      qa[ks][3] = r1 < a.group ? *reinterpret_cast<const uint32_t*>(qb + r1 * kHeadDim + d + 8) : 0u;
+      qa[ks][0] = ok0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * kHeadDim + d) : 0u;
+      qa[ks][1] = ok1 ? *reinterpret_cast<const uint32_t*>(qb + r1 * kHeadDim + d) : 0u;
+      qa[ks][2] = ok0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * kHeadDim + d + 8) : 0u;
+      qa[ks][3] = ok1 ? *reinterpret_cast<const uint32_t*>(qb + r1 * kHeadDim + d + 8) : 0u;
     }
   }
 
@@ -311,8 +329,9 @@ __global__ void __launch_bounds__(kThreads)
   for (int dn = 0; dn < 8; ++dn)
 #pragma unroll
     for (int e = 0; e < 4; ++e) st.o[dn][e] = 0.f;
-  if (c == 0 && warp == 0) {
-    // The sink enters as the initial running max with running sum 1, once.
+  if (c == 0 && head_ok) {
+    // The sink enters as the initial running max with running sum 1, in the
+    // first chunk only (one quad lane carries the 1).
     st.m0 = r0 < a.group ? a.sinks[head0 + r0] * kLog2e : -INFINITY;
     st.m1 = r1 < a.group ? a.sinks[head0 + r1] * kLog2e : -INFINITY;
     st.d0 = st.w0 = (lane & 3) == 0 ? 1.f : 0.f;
@@ -323,18 +342,19 @@ __global__ void __launch_bounds__(kThreads)
     const int stage = it % kStages;
     const bool ready = mbar_wait(&bars->full[stage], (it / kStages) & 1, &bars->abort_word, a.err_flag);
     if (!__all_sync(0xffffffffu, ready)) break;
-    const int u = u0 + it * kUnitsPerStage + warp;
-    if (u < u1 && ((bars->unit_ok[stage] >> warp) & 1u)) {
+    if (head_ok && bars->unit_ok[stage]) {
+      const int u = u0 + it;
       const uint32_t k_base = smem_addr(ring + stage * kStageBytes + warp * kUnitBytes);
-      const uint32_t v_base = k_base + kUnitsPerStage * kUnitBytes;
+      const uint32_t v_base = k_base + kHalfBytes;
       const int n_valid = min(kUnitTokens, kv_len - u * kUnitTokens);
       consume_unit<kTwoRows>(k_base, v_base, n_valid, qa, a.scale_log2, st);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->empty[stage]);
   }
+  if (!head_ok) return;
 
-  // ---- merge the four warps' states (shared memory reused after the ring drained)
+  // ---- this warp holds its head's whole state: reduce the quad's sums, write
   st.d0 += __shfl_xor_sync(0xffffffffu, st.d0, 1);
   st.d0 += __shfl_xor_sync(0xffffffffu, st.d0, 2);
   st.d1 += __shfl_xor_sync(0xffffffffu, st.d1, 1);
@@ -343,68 +363,32 @@ __global__ void __launch_bounds__(kThreads)
   st.w0 += __shfl_xor_sync(0xffffffffu, st.w0, 2);
   st.w1 += __shfl_xor_sync(0xffffffffu, st.w1, 1);
   st.w1 += __shfl_xor_sync(0xffffffffu, st.w1, 2);
-  named_barrier_sync(1, kConsumerWarps * 32);  // every consumer is done reading the ring
-
-  float* sm_o = reinterpret_cast<float*>(ring);                  // [warp][16][64]
-  float* sm_m = sm_o + kConsumerWarps * 16 * kHeadDim;          // [warp][16]
-  float* sm_d = sm_m + kConsumerWarps * 16;                     // [warp][16]
-  float* sm_w = sm_d + kConsumerWarps * 16;                     // [warp][16]
-  {
-    float* ow = sm_o + warp * 16 * kHeadDim;
-    const int col = 2 * (lane & 3);
-#pragma unroll
-    for (int dn = 0; dn < 8; ++dn) {
-      *reinterpret_cast<float2*>(ow + r0 * kHeadDim + dn * 8 + col) = make_float2(st.o[dn][0], st.o[dn][1]);
-      if (kTwoRows)
-        *reinterpret_cast<float2*>(ow + r1 * kHeadDim + dn * 8 + col) = make_float2(st.o[dn][2], st.o[dn][3]);
-    }
-    if ((lane & 3) == 0) {
-      sm_m[warp * 16 + r0] = st.m0;
-      sm_d[warp * 16 + r0] = st.d0;
-      sm_w[warp * 16 + r0] = st.w0;
-      sm_m[warp * 16 + r1] = st.m1;
-      sm_d[warp * 16 + r1] = st.d1;
-      sm_w[warp * 16 + r1] = st.w1;
-    }
-  }
-  named_barrier_sync(1, kConsumerWarps * 32);
-
   const bool direct = n_chunks == 1;
-  for (int idx = threadIdx.x; idx < a.group * 16; idx += kConsumerWarps * 32) {
-    const int row = idx >> 4, d4 = (idx & 15) * 4;
-    float m = -INFINITY;
+  const int col = 2 * (lane & 3);
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, sm_m[w * 16 + row]);
-    float den = 0.f, wden = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float mw = sm_m[w * 16 + row];
-      const float sc = mw == -INFINITY ? 0.f : fast_exp2(mw - m);
-      den += sm_d[w * 16 + row] * sc;
-      wden += sm_w[w * 16 + row] * sc;
-      const float4 ov = *reinterpret_cast<const float4*>(sm_o + (w * 16 + row) * kHeadDim + d4);
-      acc.x += ov.x * sc;
-      acc.y += ov.y * sc;
-      acc.z += ov.z * sc;
-      acc.w += ov.w * sc;
-    }
+  for (int half = 0; half < (kTwoRows ? 2 : 1); ++half) {
+    const int row = half ? r1 : r0;
+    if (row >= a.group) continue;
+    const float m = half ? st.m1 : st.m0;
+    const float den = half ? st.d1 : st.d0;
+    const float wden = half ? st.w1 : st.w0;
     const float inv = wden > 0.f ? 1.f / wden : 0.f;
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
     const float lse = (den > 0.f && m != -INFINITY) ? (m + __log2f(den)) * kLn2 : -INFINITY;
     const long long grow = static_cast<long long>(b) * a.Hq + head0 + row;
     if (direct) {
-      uint2 packed;
-      packed.x = pack_bf16x2(acc.x, acc.y);
-      packed.y = pack_bf16x2(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim + d4) = packed;
-      if (a.lse && d4 == 0) a.lse[grow] = lse;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim;
+#pragma unroll
+      for (int dn = 0; dn < 8; ++dn)
+        *reinterpret_cast<uint32_t*>(orow + dn * 8 + col) =
+            pack_bf16x2(st.o[dn][2 * half] * inv, st.o[dn][2 * half + 1] * inv);
+      if (a.lse && (lane & 3) == 0) a.lse[grow] = lse;
     } else {
-      *reinterpret_cast<float4*>(a.o_part + (grow * a.s_stride + c) * kHeadDim + d4) = acc;
-      if (d4 == 0) a.lse_part[grow * a.s_stride + c] = lse;
+      float* prow = a.o_part + (grow * a.s_stride + c) * kHeadDim;
+#pragma unroll
+      for (int dn = 0; dn < 8; ++dn)
+        *reinterpret_cast<float2*>(prow + dn * 8 + col) =
+            make_float2(st.o[dn][2 * half] * inv, st.o[dn][2 * half + 1] * inv);
+      if ((lane & 3) == 0) a.lse_part[grow * a.s_stride + c] = lse;
     }
   }
 }
@@ -413,7 +397,7 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& k_map,
                                const CUtensorMap& v_map, cudaStream_t stream) {
-  dim3 grid(a.max_chunks, a.Hkv, a.B);
+  dim3 grid(a.max_chunks, (a.Hkv + kHeadsPerCta - 1) / kHeadsPerCta, a.B);
   if (a.group > 8) {
     auto kern = decode_split_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);

@@ -10,6 +10,7 @@ namespace attn_sink {
 
 constexpr int kHeadDim = 64;     // the only head dimension the kernels are built for
 constexpr int kUnitTokens = 16;  // keys per TMA box: one 16-row slice of a page
+constexpr int kHeadsPerCta = 4;  // decode: KV heads per CTA (one TMA box covers them)
 
 // ------------------------------------------------------------- bf16 decode
 struct DecodeArgs {
