@@ -42,11 +42,11 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "cc177fbe2bed010e41c53390b21f85b0a423c3957b6eea3a7669081facc3673b",
-                "bytes": 810618368},
+                "sha256": "fb854dc7cb1db67742e12ea13270accbe19557aad0ca6a96e77cd47579f9f8c6",
+                "bytes": 814407680},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
-               "sha256": "a22883ce5ebe4619948a44cd84545bc5aec03c505024729e702058f38d66db86",
-               "bytes": 583284480},
+               "sha256": "30f902852aee24668abe2b90b6a2223d5e0aaf9ad6bbec78c12fe8f58a361c42",
+               "bytes": 584653568},
 }
 
 
