@@ -63,6 +63,15 @@ def test_prefill_many_heads_global_sinks(cuda_lib):
     _check_all(cuda_lib, _batch(32, [40, 9], prefix=[0, 20], Hq=288, Hkv=18), "288 heads")
 
 
+def test_prefill_multi_token_verify(cuda_lib):
+    """Speculative-decoding verification: 2..5 new tokens per sequence over prefixes of
+    1k..5k keys (bottom-right causal), 24 sequences, Hq 64 / Hkv 8."""
+    rng = np.random.default_rng(33)
+    q_lens = rng.integers(2, 6, 24)
+    prefix = rng.integers(1000, 5000, 24)
+    _check_all(cuda_lib, _batch(33, q_lens, prefix=prefix), "multi-token verify")
+
+
 def test_prefill_non_causal(cuda_lib):
     batch = _batch(23, [50, 129], prefix=[10, 60], causal=False)
     _check_all(cuda_lib, batch, "non-causal")
