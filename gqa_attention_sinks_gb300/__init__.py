@@ -33,6 +33,8 @@ SIGNATURES = {
     "attn_sink_prefill": ([_vp] * 10 + [_i32] * 8 + [_f32, _i32, _i32, _vp, _vp], _i32),
     "attn_sink_decode": ([_vp] * 5 + [_i32, _vp, _vp, _vp] + [_i32] * 6 + [_f32, _i32, _i32, _vp,
                                                                          _vp, _sz, _vp], _i32),
+    "attn_sink_decode_append": ([_vp] * 7 + [_i32, _vp, _vp, _vp] + [_i32] * 6 +
+                                [_f32, _i32, _i32, _vp, _vp, _sz, _vp], _i32),
     "attn_sink_decode_workspace_size": ([_i32] * 7, _sz),
     "attn_sink_decode_static_scratch": ([_vp] * 5 + [_i32, _vp, _vp, _vp] + [_i32] * 6 +
                                         [_f32, _i32, _i32, _vp, _vp], _i32),
@@ -140,6 +142,44 @@ def decode(q, k_cache, v_cache, kv_lens, block_table, sinks, *, scale=None, num_
                               B, Hq, Hkv, D, page_size, num_pages, scale, int(num_splits), dt,
                               _ptr(err_flag), _ptr(workspace), ws_bytes, _stream(stream))
     _check("attn_sink_decode", st)
+    return out, lse
+
+
+def decode_append(q, k_new, v_new, k_cache, v_cache, kv_lens, block_table, sinks, *, scale=None,
+                  num_splits=0, out=None, lse=None, workspace=None, err_flag=None, stream=None):
+    """One decode step that first writes k_new / v_new [B, Hkv, D] into the cache slot
+    of position kv_lens[b] - 1, then attends over keys 0..kv_lens[b]-1 (the caches are
+    updated in place).  Returns (out, lse) like ``decode``."""
+    lib = load()
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache),
+                    ("v_cache", v_cache)):
+        _dev(t, name, q.dtype)
+    _dev(kv_lens, "kv_lens", torch.int32)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(sinks, "sinks", torch.float32)
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+        raise ValueError("k_new / v_new must be [B, Hkv, D] = %s" % ((B, Hkv, D),))
+    bt_stride = block_table.shape[1]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _dev(out, "out", q.dtype)
+    _dev(lse, "lse", torch.float32)
+    need = decode_workspace_size(B, Hq, Hkv, D, bt_stride, page_size, num_splits)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.attn_sink_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(kv_lens), _ptr(block_table), bt_stride, _ptr(sinks),
+                                     _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size, num_pages,
+                                     scale, int(num_splits), dt, _ptr(err_flag), _ptr(workspace),
+                                     ws_bytes, _stream(stream))
+    _check("attn_sink_decode_append", st)
     return out, lse
 
 

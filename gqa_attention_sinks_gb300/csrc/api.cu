@@ -175,12 +175,17 @@ ATTN_SINK_API size_t attn_sink_decode_workspace_size(int32_t B, int32_t Hq, int3
   return partial_bytes(static_cast<long long>(B) * Hq, p.s_stride, nullptr);
 }
 
-ATTN_SINK_API attn_sink_status attn_sink_decode(
-    const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_lens,
-    const int32_t* block_table, int32_t block_table_stride, const float* sinks, void* out,
-    float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
-    int32_t num_pages, float scale, int32_t num_splits, attn_sink_dtype dtype, int32_t* err_flag,
-    void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Decode, optionally appending the step's key and value first (k_new != null).
+attn_sink_status decode_impl(
+    const void* q, const void* k_new, const void* v_new, const void* k_cache, const void* v_cache,
+    const int32_t* kv_lens, const int32_t* block_table, int32_t block_table_stride,
+    const float* sinks, void* out, float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+    int32_t page_size, int32_t num_pages, float scale, int32_t num_splits, attn_sink_dtype dtype,
+    int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream) {
   attn_sink_status st =
       check_shapes(B, Hq, Hkv, D, page_size, num_pages, block_table_stride, dtype);
   if (st != ATTN_SINK_OK) return st;
@@ -200,6 +205,24 @@ ATTN_SINK_API attn_sink_status attn_sink_decode(
     if (need && (!workspace || workspace_bytes < need ||
                  (reinterpret_cast<uintptr_t>(workspace) & 255u)))
       return ATTN_SINK_ERR_WORKSPACE;
+    if (k_new) {
+      AppendArgs ap{};
+      ap.k_new = k_new;
+      ap.v_new = v_new;
+      ap.k_cache = const_cast<void*>(k_cache);
+      ap.v_cache = const_cast<void*>(v_cache);
+      ap.kv_lens = kv_lens;
+      ap.block_table = block_table;
+      ap.err_flag = err_flag;
+      ap.B = B;
+      ap.Hkv = Hkv;
+      ap.bt_stride = block_table_stride;
+      ap.page_size = page_size;
+      ap.num_pages = num_pages;
+      ap.elem_bytes = 4;
+      cudaError_t e = launch_append(ap, s);
+      if (e != cudaSuccess) return from_cuda(e);
+    }
     SimtArgs a{};
     a.q = static_cast<const float*>(q);
     a.k_cache = static_cast<const float*>(k_cache);
@@ -274,6 +297,10 @@ ATTN_SINK_API attn_sink_status attn_sink_decode(
   a.chunk_units = p.chunk_units;
   a.max_chunks = p.max_chunks;
   a.s_stride = p.s_stride;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache_w = k_new ? const_cast<void*>(k_cache) : nullptr;
+  a.v_cache_w = k_new ? const_cast<void*>(v_cache) : nullptr;
   cudaError_t e = launch_decode_bf16(a, k_map, v_map, s);
   if (e != cudaSuccess || p.s_stride == 0) return from_cuda(e);
 
@@ -292,6 +319,33 @@ ATTN_SINK_API attn_sink_status attn_sink_decode(
     m.chunk_units = p.chunk_units;
   }
   return from_cuda(launch_merge(m, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+ATTN_SINK_API attn_sink_status attn_sink_decode(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_lens,
+    const int32_t* block_table, int32_t block_table_stride, const float* sinks, void* out,
+    float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+    int32_t num_pages, float scale, int32_t num_splits, attn_sink_dtype dtype, int32_t* err_flag,
+    void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, nullptr, nullptr, k_cache, v_cache, kv_lens, block_table,
+                     block_table_stride, sinks, out, lse, B, Hq, Hkv, D, page_size, num_pages,
+                     scale, num_splits, dtype, err_flag, workspace, workspace_bytes, stream);
+}
+
+ATTN_SINK_API attn_sink_status attn_sink_decode_append(
+    const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    const int32_t* kv_lens, const int32_t* block_table, int32_t block_table_stride,
+    const float* sinks, void* out, float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+    int32_t page_size, int32_t num_pages, float scale, int32_t num_splits, attn_sink_dtype dtype,
+    int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return ATTN_SINK_ERR_INVALID_ARG;
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, kv_lens, block_table, block_table_stride,
+                     sinks, out, lse, B, Hq, Hkv, D, page_size, num_pages, scale, num_splits, dtype,
+                     err_flag, workspace, workspace_bytes, stream);
 }
 
 ATTN_SINK_API attn_sink_status attn_sink_merge(const float* o_parts, const float* lse_parts,

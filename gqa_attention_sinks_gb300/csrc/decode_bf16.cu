@@ -20,7 +20,12 @@
 //               query heads (M = 16 rows) come from mma.sync m16n8k16 bf16
 //               with fp32 accumulation, the online softmax runs in registers,
 //               and P*V reuses the score fragments as the A operand.
-// Each warp writes either its heads' final output (the sequence has one
+// In append mode the producer of the CTA whose chunk holds a sequence's last
+// position first writes the step's key and value rows of its heads there
+// ("Accelerating Sonar through speculation", section "Inferensi dengan
+// Speculative Decoding": pages for each sequence's next token are allocated
+// before the step).
+// Each warp writes either its head's final output (the sequence has one
 // chunk) or an fp32 partial (o, lse) that the merge kernel combines.
 //
 // The kernel is HBM-bound: per key and KV head it moves 256 B and does
@@ -261,6 +266,36 @@ __global__ void __launch_bounds__(kThreads)
         tok = (u % units_per_page) * kUnitTokens;
       }
     };
+    if (a.k_new && kv_len >= 1) {
+      // Append mode: the CTA whose chunk holds the last position writes the
+      // step's key and value rows of its heads there before any copy of that
+      // unit is issued; the proxy fences order the generic writes before the
+      // TMA reads.
+      const int unit_last = (kv_len - 1) / kUnitTokens;
+      if (unit_last >= u0 && unit_last < u1) {
+        const int pos = kv_len - 1;
+        const int phys = bt_row[pos / a.page_size];
+        if (phys >= 0 && phys < a.num_pages) {
+          const long long row = static_cast<long long>(phys) * a.page_size + pos % a.page_size;
+          constexpr int kPieces = kHeadDim * 2 / 16;  // 16-byte pieces of one head's row
+          for (int i = lane; i < 2 * kHeadsPerCta * kPieces; i += 32) {
+            const int t = i / (kHeadsPerCta * kPieces), h = (i / kPieces) % kHeadsPerCta,
+                      piece = i % kPieces;
+            const int g = g0 + h;
+            if (g < a.Hkv) {
+              const uint4* src = reinterpret_cast<const uint4*>(t ? a.v_new : a.k_new) +
+                                 (static_cast<long long>(b) * a.Hkv + g) * kPieces + piece;
+              uint4* dst = reinterpret_cast<uint4*>(t ? a.v_cache_w : a.k_cache_w) +
+                           (row * a.Hkv + g) * kPieces + piece;
+              *dst = *src;
+            }
+          }
+          fence_proxy_async_global();
+        }
+      }
+      __syncwarp();
+      fence_proxy_async_global();
+    }
     int cur_phys, cur_tok, nxt_phys, nxt_tok;
     fetch(0, cur_phys, cur_tok);
     fetch(32, nxt_phys, nxt_tok);

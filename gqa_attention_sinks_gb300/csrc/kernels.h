@@ -30,10 +30,32 @@ struct DecodeArgs {
   int chunk_units;             // 16-key units per chunk when num_splits == 0
   int max_chunks;              // grid.x
   int s_stride;                // partial slots per row in o_part / lse_part
+  // Append mode (all null otherwise): before its keys are read, the step's
+  // k_new / v_new [B, Hkv, 64] go into the slot of position kv_len - 1.
+  const void* k_new;
+  const void* v_new;
+  void* k_cache_w;
+  void* v_cache_w;
 };
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& k_map,
                                const CUtensorMap& v_map, cudaStream_t stream);
+
+// ------------------------------------------------------------- KV append
+// Writes k_new / v_new [B, Hkv, 64] into the cache slot of position
+// kv_lens[b] - 1 of every sequence with kv_lens[b] >= 1 (any element size).
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* kv_lens;
+  const int32_t* block_table;
+  int32_t* err_flag;
+  int B, Hkv, bt_stride, page_size, num_pages, elem_bytes;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------- merge
 struct MergeArgs {

@@ -134,6 +134,33 @@ ATTN_SINK_API attn_sink_status attn_sink_decode(const void* q, const void* k_cac
                                   int32_t num_splits, attn_sink_dtype dtype, int32_t* err_flag,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * One decode step that first appends the step's key and value.  "Accelerating
+ * Sonar through speculation", section "Inferensi dengan Speculative Decoding":
+ * before a step runs, pages in the KV cache are allocated for each sequence's
+ * next token.  For every sequence b with kv_lens[b] >= 1, k_new[b] and v_new[b]
+ * are written into the cache slot of position kv_lens[b] - 1 (page
+ * block_table[b, (kv_lens[b]-1) / page_size], row (kv_lens[b]-1) % page_size,
+ * every KV head), then attention runs over keys 0..kv_lens[b]-1 exactly as
+ * attn_sink_decode does.  The result equals writing the slot and calling
+ * attn_sink_decode; in bf16 the write happens inside the decode launch.
+ *
+ *  k_new, v_new device [B, Hkv, D] dtype, 16-byte aligned (INVALID_ARG if NULL).
+ *  k_cache, v_cache are written (only the B appended slots).
+ *  A slot whose page index is outside [0, num_pages), or beyond the table row,
+ *  is not written and sets *err_flag |= ATTN_SINK_FLAG_BAD_PAGE.
+ * Every other argument, the workspace (attn_sink_decode_workspace_size) and
+ * the errors are those of attn_sink_decode.
+ */
+ATTN_SINK_API attn_sink_status attn_sink_decode_append(const void* q, const void* k_new, const void* v_new,
+                                         void* k_cache, void* v_cache, const int32_t* kv_lens,
+                                         const int32_t* block_table, int32_t block_table_stride,
+                                         const float* sinks, void* out, float* lse, int32_t B,
+                                         int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                                         int32_t num_pages, float scale, int32_t num_splits,
+                                         attn_sink_dtype dtype, int32_t* err_flag, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
 /* Workspace bytes attn_sink_decode needs for these arguments (0 when it needs
  * none).  Pure host function. */
 ATTN_SINK_API size_t attn_sink_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
