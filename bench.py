@@ -42,11 +42,11 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "fb854dc7cb1db67742e12ea13270accbe19557aad0ca6a96e77cd47579f9f8c6",
+                "sha256": "385fb73d202cd7c8b5a386141d0e075ae908aeb3fa27bea8940220a552e8472a",
                 "bytes": 814407680},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
-               "sha256": "30f902852aee24668abe2b90b6a2223d5e0aaf9ad6bbec78c12fe8f58a361c42",
-               "bytes": 584653568},
+               "sha256": "c8f683650c6ff598c571742d7e6fa0aaf0154be587091fad083eb77abb5f0a5b",
+               "bytes": 584773632},
 }
 
 
