@@ -57,6 +57,17 @@ def test_decode_edge_lengths(cuda_lib):
         assert db.err.item() == 0
 
 
+def test_decode_max_splits(cuda_lib):
+    """num_splits = 256 (the maximum): most chunks of these sequences are empty pages
+    ranges and only chunk 0 carries the sink."""
+    batch = _small_decode(seed=9, num_seqs=4, kv=(1, 4100))
+    db = DeviceBatch(batch)
+    out, lse = _decode(cuda_lib, db, 256)
+    ref, ref_lse, _ = oracle_problem(batch).attention()
+    compare(out, lse, ref, ref_lse, what="decode S=256")
+    assert db.err.item() == 0
+
+
 def test_decode_split_invariance_and_determinism(cuda_lib):
     batch = _small_decode(seed=8, num_seqs=5, kv=(200, 2000))
     db = DeviceBatch(batch)

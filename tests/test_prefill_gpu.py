@@ -72,6 +72,20 @@ def test_prefill_multi_token_verify(cuda_lib):
     _check_all(cuda_lib, _batch(33, q_lens, prefix=prefix), "multi-token verify")
 
 
+def test_prefill_one_long_sequence_sampled(cuda_lib):
+    """One 16384-token causal prefill (rows see up to 128 key tiles), Hq 64 / Hkv 8:
+    sampled rows plus both ends of the sequence."""
+    batch = _batch(34, [16384])
+    db = DeviceBatch(batch)
+    out, lse = _prefill(cuda_lib, db)
+    rows = W.sample_rows(np.random.default_rng(34), batch, 768)
+    ends = np.concatenate([np.arange(t * 64, (t + 1) * 64) for t in (0, 1, 16382, 16383)])
+    rows = np.unique(np.concatenate([rows, ends]))
+    ref, ref_lse, _ = oracle_problem(batch).attention(rows)
+    compare(out, lse, ref, ref_lse, rows=rows, what="one long prefill")
+    assert db.err.item() == 0
+
+
 def test_prefill_non_causal(cuda_lib):
     batch = _batch(23, [50, 129], prefix=[10, 60], causal=False)
     _check_all(cuda_lib, batch, "non-causal")
