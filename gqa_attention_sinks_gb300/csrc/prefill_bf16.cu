@@ -14,7 +14,7 @@
 // query block of every sequence, then the one before, ...), so the rows with
 // the most keys start first and every CTA ends on short ones.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warps 0-3  softmax for Q tile 0, warps 4-7 softmax for Q tile 1: one
 //              thread per row; S comes out of TMEM with tcgen05.ld, the row
 //              max/exp2/sum run in registers, P (bf16) goes back into TMEM in
