@@ -85,8 +85,10 @@ typedef enum {
  *  k_cache, v_cache device [num_pages, page_size, Hkv, D] dtype.
  *  cu_seqlens_q device int32 [B+1], non-decreasing, cu_seqlens_q[0] = 0,
  *               cu_seqlens_q[B] = total_q.
- *  kv_lens      device int32 [B]: keys of sequence b, new tokens included
- *               (kv_len >= q_len when causal).
+ *  kv_lens      device int32 [B]: keys of sequence b, new tokens included.
+ *               Causal rows are bottom-right aligned: row i of a sequence sits
+ *               at position kv_len - q_len + i; when kv_len < q_len the rows
+ *               before position 0 see no key (out = 0, lse = the sink).
  *  block_table  device int32 [B, block_table_stride]; entries for pages at or
  *               beyond ceil(kv_len / page_size) are never read.
  *  sinks        device fp32 [Hq].

@@ -86,6 +86,19 @@ def test_prefill_one_long_sequence_sampled(cuda_lib):
     assert db.err.item() == 0
 
 
+def test_prefill_rows_before_first_key(cuda_lib):
+    """Causal with kv_len < q_len: bottom-right aligned, the first q_len - kv_len rows
+    of a sequence see no key at all (out 0, lse = sink), including a whole tile."""
+    rng = np.random.default_rng(35)
+    q_lens = np.array([40, 10, 20, 300])
+    kv = np.array([30, 3, 20, 100])
+    pool = W.make_pool(rng, kv, 8, 64, 16, W.BF16)
+    sinks = W.sinks_normal(rng, 64, 2.0)
+    q = W.make_queries(rng, int(q_lens.sum()), 64, 64, W.BF16)
+    _check_all(cuda_lib, W.batch_from_pool(pool, np.arange(4), q_lens, q, sinks),
+               "rows before the first key")
+
+
 def test_prefill_non_causal(cuda_lib):
     batch = _batch(23, [50, 129], prefix=[10, 60], causal=False)
     _check_all(cuda_lib, batch, "non-causal")
