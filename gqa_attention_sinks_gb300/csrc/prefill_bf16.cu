@@ -569,16 +569,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_valid) {
         const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
         const long long grow = static_cast<long long>(w.q_start + tok) * a.Hq + head;
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim);
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim;
+        if ((reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) {
+          // 32-byte stores: whole sectors, four instructions per row.
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const int h = v >> 2, i = (v & 3) * 8;
-          uint4 o4;
-          o4.x = pack_bf16x2(__uint_as_float(o[h][i + 0]) * inv, __uint_as_float(o[h][i + 1]) * inv);
-          o4.y = pack_bf16x2(__uint_as_float(o[h][i + 2]) * inv, __uint_as_float(o[h][i + 3]) * inv);
-          o4.z = pack_bf16x2(__uint_as_float(o[h][i + 4]) * inv, __uint_as_float(o[h][i + 5]) * inv);
-          o4.w = pack_bf16x2(__uint_as_float(o[h][i + 6]) * inv, __uint_as_float(o[h][i + 7]) * inv);
-          dst[v] = o4;
+          for (int v = 0; v < 4; ++v) {
+            const int h = v >> 1, i = (v & 1) * 16;
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(o[h][i + 2 * e]) * inv, __uint_as_float(o[h][i + 2 * e + 1]) * inv);
+            st_global_v8(orow + v * 16, pk);
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const int h = v >> 2, i = (v & 3) * 8;
+            uint4 o4;
+            o4.x = pack_bf16x2(__uint_as_float(o[h][i + 0]) * inv, __uint_as_float(o[h][i + 1]) * inv);
+            o4.y = pack_bf16x2(__uint_as_float(o[h][i + 2]) * inv, __uint_as_float(o[h][i + 3]) * inv);
+            o4.z = pack_bf16x2(__uint_as_float(o[h][i + 4]) * inv, __uint_as_float(o[h][i + 5]) * inv);
+            o4.w = pack_bf16x2(__uint_as_float(o[h][i + 6]) * inv, __uint_as_float(o[h][i + 7]) * inv);
+            dst[v] = o4;
+          }
         }
         if (a.lse)
           a.lse[grow] = (d_run > 0.f && m_run != -INFINITY) ? (m_run + __log2f(d_run)) * kLn2 : -INFINITY;

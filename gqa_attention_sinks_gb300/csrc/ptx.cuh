@@ -229,6 +229,14 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 256-bit global store (the address must be 32-byte aligned): whole 32-byte
+// sectors per lane, half the store instructions of 16-byte stores.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // True in exactly one active lane of the warp (warp-collective).
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;
