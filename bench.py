@@ -43,8 +43,8 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "28a4cb470fe98643f2853788006c1a12b0fb2f41bad60dcddf33cf79387502ae",
-                "bytes": 839086592},
+                "sha256": "81aa7d691364c509b7493a3a5fddd8c8cb026f3732242e2927f1bda42c375c65",
+                "bytes": 881344512},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
                "sha256": "c8f683650c6ff598c571742d7e6fa0aaf0154be587091fad083eb77abb5f0a5b",
                "bytes": 584773632},
