@@ -302,8 +302,15 @@ def run_ours(args, ws, rank, local):
         }
 
     # ---------------------------------------------------------- prefill
-    if args.workload in ("decode", "prefill") and not args.no_prefill:
-        pre = W.gptoss_prefill(seed=20260003 + seed_off)
+    if (args.workload in ("decode", "prefill", "mixed")) and not args.no_prefill:
+        if args.workload == "mixed":
+            pre = W.mixed_batch(seed=20260005 + seed_off)["prefill"]
+            pre_name = ("mixed batch, chunked-prefill part: 4 x 512 new tokens over prefixes "
+                        "U[0, 16384], Hq 64, Hkv 8, D 64, bf16, paged K/V, 1% outlier keys")
+        else:
+            pre = W.gptoss_prefill(seed=20260003 + seed_off)
+            pre_name = ("gpt-oss causal prefill: 8 seqs x 4096, Hq 64, Hkv 8, D 64, bf16, "
+                        "ragged cu_seqlens, paged K/V")
         q, k, v = to_dev(pre.q), to_dev(pre.k_cache), to_dev(pre.v_cache)
         cu, kvl = to_dev(pre.cu_seqlens_q), to_dev(pre.kv_lens)
         bt, sinks = to_dev(pre.block_table), to_dev(pre.sinks)
@@ -315,8 +322,7 @@ def run_ours(args, ws, rank, local):
                         out=out, lse=lse)
 
         flops = prefill_flops(pre)
-        part = {"workload": "gpt-oss causal prefill: 8 seqs x 4096, Hq 64, Hkv 8, D 64, bf16, "
-                            "ragged cu_seqlens, paged K/V", "flops_per_step": flops}
+        part = {"workload": pre_name, "flops_per_step": flops}
         try:
             pstep()
             torch.cuda.synchronize()
@@ -337,7 +343,9 @@ def run_ours(args, ws, rank, local):
                          "ms_per_step": round(pms, 4), "steps": psteps, "clocks": pclocks,
                          "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak,
                                       "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                                      "traffic": ncu_traffic("prefill"), "peak_source": pk_kind}})
+                                      "traffic": (ncu_traffic("prefill") if args.workload != "mixed"
+                                                  else None),
+                                      "peak_source": pk_kind}})
         except gas.AttnSinkError as e:
             part.update({"unavailable": str(e)})
         if result:
