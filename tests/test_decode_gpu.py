@@ -44,6 +44,19 @@ def test_decode_group_sizes(cuda_lib, group, Hkv):
         compare(out, lse, ref, ref_lse, what="group %d S=%d" % (group, S))
 
 
+@pytest.mark.parametrize("Hq", [8, 16])
+def test_decode_single_kv_head(cuda_lib, Hq):
+    """Multi-query attention (Hkv = 1): the 4-head TMA box reaches past the tensor's
+    head dimension, whose missing heads TMA fills with zeros."""
+    batch = _small_decode(seed=12, num_seqs=5, kv=(1, 900), Hq=Hq, Hkv=1)
+    db = DeviceBatch(batch)
+    ref, ref_lse, _ = oracle_problem(batch).attention()
+    for S in (0, 3):
+        out, lse = _decode(cuda_lib, db, S)
+        compare(out, lse, ref, ref_lse, what="MQA decode Hq %d S=%d" % (Hq, S))
+    assert db.err.item() == 0
+
+
 def test_decode_edge_lengths(cuda_lib):
     """kv_len 0 (out 0, lse = sink), 1, page boundaries and ragged tails."""
     lens = [0, 1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 511, 512, 513]

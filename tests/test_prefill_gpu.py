@@ -110,6 +110,11 @@ def test_prefill_group_sizes(cuda_lib, group, Hkv):
                "group %d" % group)
 
 
+def test_prefill_single_kv_head(cuda_lib):
+    """Multi-query attention: one KV head, 16 query heads (group 16)."""
+    _check_all(cuda_lib, _batch(36, [90, 33], prefix=[0, 200], Hq=16, Hkv=1), "MQA prefill")
+
+
 def test_prefill_sink_extremes(cuda_lib):
     """Sinks -inf, -4, 0, 4, 8 and large: sink=-inf is plain attention, large sinks
     push the output toward 0."""
