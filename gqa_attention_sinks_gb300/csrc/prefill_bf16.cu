@@ -92,7 +92,7 @@ struct alignas(8) Bars {
   uint64_t q_empty[kQBufs];   // both Q tiles' MMAs of the buffer's work tile are done
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full[kQTiles];   // S is in TMEM
+  uint64_t s_full[kQTiles];   // S is in TMEM, and s_uok holds its stage's unit mask
   uint64_t s_free[kQTiles];   // the warpgroup has loaded S; S may be overwritten
   uint64_t p_ready[kQTiles];  // P is in TMEM (and O rescaled)
   uint64_t pv_done[kQTiles];  // P*V has completed: P may be overwritten, O is current
@@ -100,6 +100,7 @@ struct alignas(8) Bars {
   uint64_t exp_turn[kQTiles]; // warpgroup q may run its exponentials (token passed between them)
   uint64_t mma_done;
   uint32_t unit_ok[kStages];  // bit u: 16-key unit u of the stage's tile was loaded
+  uint32_t s_uok[kQTiles];    // unit_ok of the stage the current S was computed from
   uint32_t tmem_base;
   int abort_word;
 };
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_empty[s], kQTiles);  // released by every Q tile's P*V
     }
     for (int q = 0; q < kQTiles; ++q) {
-      mbar_init(&bars->s_full[q], 1);
+      mbar_init(&bars->s_full[q], 2);   // the MMA commit and the MMA leader's s_uok arrive
       mbar_init(&bars->s_free[q], 4);   // one arrive per softmax warp
       mbar_init(&bars->p_ready[q], 4);
       mbar_init(&bars->pv_done[q], 1);
@@ -299,6 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ss(tmem_s, q_desc0 + qb * kQBufDesc + kk * 2, k_desc0 + st * kStageDesc + kk * 2, kIdescS,
                   kk > 0);
         umma_commit(&bars->s_full[q]);
+        // The stage's unit mask travels with S: this warp has waited for the
+        // stage's kv_full, and the plain arrive releases the copy, so the
+        // softmax needs no kv_full wait of its own.  The previous S (and its
+        // mask) has been read: this issue followed its s_free.
+        bars->s_uok[q] = bars->unit_ok[st];
+        mbar_arrive(&bars->s_full[q]);
       }
       __syncwarp();
     };
@@ -386,13 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < w.n_kv; ++j) {
         const int cur = kv_it + j, u = it + j;
         const int st = cur % kStages;
-        bool ready = mbar_wait(&bars->s_full[q], u & 1, abort_word, a.err_flag);
-        // S was computed from this stage, so its load phase has completed; the
-        // wait returns at once and orders the producer's unit_ok write before the read.
-        ready = ready && mbar_wait(&bars->kv_full[st], (cur / kStages) & 1, abort_word, a.err_flag);
+        // s_full completes after the MMA warp saw the stage's kv_full: the
+        // stage has landed, and s_uok holds its unit mask.
+        const bool ready = mbar_wait(&bars->s_full[q], u & 1, abort_word, a.err_flag);
         ok = __all_sync(0xffffffffu, ready);
         if (!ok) break;
-        const uint32_t uok = bars->unit_ok[st];
+        const uint32_t uok = bars->s_uok[q];
         tc_fence_after_sync();
         uint32_t s[4][32];
 #pragma unroll
@@ -410,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (uok != 0xFFu || key_base + kKeys > w.kv_len) {
           // Keys this tile does not hold (past kv_len, or a skipped page) may sit
           // over stale shared memory: their P is 0, but 0 * NaN is NaN, so thread
-          // r clears V row r.  The stage has landed (kv_full above) and this
+          // r clears V row r.  The stage has landed (s_full above) and this
           // warpgroup's P*V is issued only after its p_ready below; each Q tile's
           // P*V waits only for its own warpgroup, so both clear the rows (the same
           // zeros).
