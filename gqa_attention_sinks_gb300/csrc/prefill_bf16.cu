@@ -62,6 +62,16 @@ constexpr int kSoftmaxWarps = 4 * kQTiles;
 constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kProducerWarpV = kMmaWarp + kQTiles;
 constexpr int kThreads = 32 * (kProducerWarpV + 1);
+// Registers per thread after the role split: the producer/MMA warpgroup gives
+// registers back, the two softmax warpgroups take them.  setmaxnreg.inc draws
+// on the block's launch allocation (kThreads x kLaunchRegs), so the split must
+// fit in it, or the increase would wait for ever.
+constexpr int kLaunchRegs = 168;  // what 65536 / kThreads allows, rounded down to 8
+constexpr int kSupportRegs = 72, kSoftmaxRegs = 216;
+static_assert(kThreads * kLaunchRegs <= 65536, "launch allocation");
+static_assert(128 * kSupportRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
+static_assert(kSupportRegs % 8 == 0 && kSoftmaxRegs % 8 == 0, "setmaxnreg granularity");
+static_assert(kProducerWarp % 4 == 0 && kProducerWarpV == kProducerWarp + 3, "one support warpgroup");
 constexpr uint32_t kTmemCols = 256 * kQTiles;  // S, O and P of every Q tile
 __device__ __forceinline__ uint32_t col_s(int q) { return static_cast<uint32_t>(q) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int q) { return 128u * kQTiles + static_cast<uint32_t>(q) * 64u; }
@@ -199,6 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
 
+  if (warp >= kProducerWarp) {
+    // Warpgroup 2 (both producers and both MMA warps) runs one setmaxnreg, as
+    // the instruction requires of a whole warpgroup.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSupportRegs));
   if (warp == kProducerWarp || warp == kProducerWarpV) {
     // ---------------------------------------------------------------- TMA
     const bool is_k = warp == kProducerWarp;  // else the V producer
@@ -365,7 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&bars->mma_done, 0);  // no MMA may still write TMEM at dealloc
     }
     __syncwarp();
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ---------------------------------------------------------------- softmax
     const int q = warp >> 2;
     const int wq = warp & 3;
@@ -630,6 +646,13 @@ cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  // The register split inside the kernel assumes the launch allocation; a
+  // build that launched with fewer registers would make setmaxnreg.inc wait
+  // for ever, so it is refused here instead.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, prefill_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   const unsigned grid = static_cast<unsigned>(n_tiles < sms ? n_tiles : sms);
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, a, n_tiles);
   return cudaGetLastError();
