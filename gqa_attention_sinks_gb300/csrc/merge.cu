@@ -8,7 +8,7 @@
 // puts the sink in the first chunk only, so it already sits inside partial 0.
 //
 // One warp per row, two head-dim elements per lane (D = 64); partials are
-// read as coalesced 256-byte lines.
+// read as coalesced 256-byte lines, kStep of them in flight at a time.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -16,12 +16,17 @@ namespace attn_sink {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kStep = 8;  // partials whose loads are in flight together
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const MergeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kWarps + warp;
+  // Launched as a programmatic dependent of the kernel that wrote the
+  // partials: wait here until that grid has completed and its writes are
+  // visible (returns at once when there is no such grid).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (row >= a.rows) return;
 
   int n = a.num_parts;
@@ -35,22 +40,32 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const MergeArgs a) {
   const float* lse_row = a.lse_part + static_cast<long long>(row) * a.s_stride;
   const float* o_row = a.o_part + static_cast<long long>(row) * a.s_stride * kHeadDim;
 
-  float m = -INFINITY;
-  for (int c = lane; c < n; c += 32) m = fmaxf(m, lse_row[c]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-
+  // Single pass with a running maximum m (log2 domain).  Each step issues the
+  // loads of kStep partials before combining any of them; waiting for each
+  // partial before loading the next would cost one memory latency per chunk.
+  float m = -INFINITY, den = 0.f;
   float2 acc = make_float2(0.f, 0.f);
-  float den = 0.f;
-  if (m != -INFINITY) {
-    const float m2 = m * kLog2e;
-    for (int c = 0; c < n; ++c) {
-      const float l = lse_row[c];
-      const float w = l == -INFINITY ? 0.f : exp2f(fmaf(l, kLog2e, -m2));
-      const float2 o = *reinterpret_cast<const float2*>(o_row + c * kHeadDim + 2 * lane);
-      den += w;
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
+  for (int cb = 0; cb < n; cb += kStep) {
+    float l[kStep];
+    float2 o[kStep];
+#pragma unroll
+    for (int k = 0; k < kStep; ++k) {
+      const bool valid = cb + k < n;
+      l[k] = valid ? lse_row[cb + k] : -INFINITY;
+      o[k] = valid ? *reinterpret_cast<const float2*>(o_row + (cb + k) * kHeadDim + 2 * lane)
+                   : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kStep; ++k) {
+      if (l[k] == -INFINITY) continue;
+      const float lk = l[k] * kLog2e;
+      const float m_new = fmaxf(m, lk);
+      const float keep = exp2f(m - m_new);  // 0 while m is -inf
+      const float w = exp2f(lk - m_new);
+      den = fmaf(den, keep, w);
+      acc.x = fmaf(acc.x, keep, w * o[k].x);
+      acc.y = fmaf(acc.y, keep, w * o[k].y);
+      m = m_new;
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -63,7 +78,7 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const MergeArgs a) {
     *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + base) =
         pack_bf16x2(acc.x, acc.y);
   }
-  if (a.lse && lane == 0) a.lse[row] = den > 0.f ? m + log2f(den) * kLn2 : -INFINITY;
+  if (a.lse && lane == 0) a.lse[row] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
 }
 
 }  // namespace
@@ -71,8 +86,20 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const MergeArgs a) {
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
   const int blocks = (a.rows + kWarps - 1) / kWarps;
-  merge_kernel<<<blocks, kWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  // Programmatic stream serialisation: the merge grid's launch overlaps the end
+  // of the previous kernel; griddepcontrol.wait above orders every partial
+  // read after that kernel has completed.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel, a);
 }
 
 }  // namespace attn_sink
