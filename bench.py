@@ -43,8 +43,8 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "81aa7d691364c509b7493a3a5fddd8c8cb026f3732242e2927f1bda42c375c65",
-                "bytes": 881344512},
+                "sha256": "dd3566de9e5d5231a74e896e85bda0b143ebfea2f20b0cace1ad3095c78f6c96",
+                "bytes": 808317184},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
                "sha256": "e432450e2f7a2466701f7b88d0a845213a66cc25fb0f8a12b0e26b1417e5df1c",
                "bytes": 584773632},
