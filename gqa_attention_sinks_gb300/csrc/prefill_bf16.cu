@@ -30,6 +30,8 @@
 //              slices of a tile take as long as the tile's MMAs; two issuing
 //              warps on different SMSPs keep the unit fed while each one
 //              computes addresses and waits on barriers.
+// Registers: setmaxnreg gives warps 8-11 72 per thread and the two softmax
+// warpgroups 216 (the launch allocation is 168 for all 384 threads).
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,320), O1 [320,384),
 // P0 [384,448), P1 [448,512) (P as packed bf16 pairs).
 //
