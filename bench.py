@@ -43,7 +43,7 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "dd3566de9e5d5231a74e896e85bda0b143ebfea2f20b0cace1ad3095c78f6c96",
+                "sha256": "dd97d5c2bb536e168ebfa58e2bb5497a6fc6bf9f719c37978cbe89d34038834e",
                 "bytes": 808317184},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
                "sha256": "e432450e2f7a2466701f7b88d0a845213a66cc25fb0f8a12b0e26b1417e5df1c",
