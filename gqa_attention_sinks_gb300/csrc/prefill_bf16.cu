@@ -9,10 +9,11 @@
 // Work tile: sequence b, KV head g and a block of 256 query rows = two Q tiles
 // of 128 rows.  A Q tile packs 128/G consecutive query tokens x the G query
 // heads of KV group g (GQA packing), so each K/V tile is read once per 2*128/G
-// tokens of the whole group.  The grid has one CTA per SM; CTA c takes work
-// tiles c, c + gridDim.x, ... from a list ordered longest rows first (the last
-// query block of every sequence, then the one before, ...), so the rows with
-// the most keys start first and every CTA ends on short ones.
+// tokens of the whole group.  The grid has one CTA per SM.  Work tiles form a
+// list ordered longest rows first (the last query block of every sequence,
+// then the one before, ...), so the rows with the most keys start first; CTA c
+// takes one tile per round of gridDim.x tiles, position c in even rounds and
+// gridDim.x - 1 - c in odd ones, which evens out the CTAs' sums.
 //
 // Warp roles (384 threads):
 //   warps 0-3  softmax for Q tile 0, warps 4-7 softmax for Q tile 1: one
@@ -132,6 +133,15 @@ struct WorkTile {
   long long first_pos;  // absolute position of the tile's first query
 };
 
+// Work tile of round `round` for this CTA.  Rounds alternate direction (CTA c
+// takes position c of even rounds and gridDim.x - 1 - c of odd ones), so a CTA
+// that drew one of the longest tiles of a round draws one of the shortest of
+// the next.  Tiles grow with the round, so a tile past n_tiles ends the loop.
+__device__ __forceinline__ long long snake_tile(long long round) {
+  const long long pos = (round & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x;
+  return round * gridDim.x + pos;
+}
+
 __device__ __forceinline__ bool decode_tile(const PrefillArgs& a, const Meta& m, long long t,
                                             int tok_per_cta, WorkTile& w) {
   const long long heads = static_cast<long long>(a.B) * a.Hkv;
@@ -228,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t reuse = l2_policy_evict_last();   // K/V tiles serve every later query block
     int qw = 0, kv_it = 0;
     bool ok = true;
-    for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+    for (long long rnd = 0, t = snake_tile(0); ok && t < n_tiles; t = snake_tile(++rnd)) {
       WorkTile w;
       if (!decode_tile(a, meta, t, tok_per_cta, w)) continue;
       if (is_k && w.kv_len < w.kv_raw && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
@@ -340,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int qw = 0, kv_it = 0, it = 0, ow = 0;
     bool ok = true;
-    for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+    for (long long rnd = 0, t = snake_tile(0); ok && t < n_tiles; t = snake_tile(++rnd)) {
       WorkTile w;
       if (!decode_tile(a, meta, t, tok_per_cta, w) || w.n_kv == 0) continue;
       const int qb = qw % kQBufs;
@@ -399,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kQTiles > 1 && q == 1 && lane == 0) mbar_arrive(&bars->exp_turn[0]);
     int kv_it = 0, it = 0;
     bool ok = true;
-    for (long long t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+    for (long long rnd = 0, t = snake_tile(0); ok && t < n_tiles; t = snake_tile(++rnd)) {
       WorkTile w;
       if (!decode_tile(a, meta, t, tok_per_cta, w)) continue;
       const int tok = w.tok0 + q * tok_per_tile + r / a.group;
