@@ -43,8 +43,8 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "dd97d5c2bb536e168ebfa58e2bb5497a6fc6bf9f719c37978cbe89d34038834e",
-                "bytes": 808317184},
+                "sha256": "409f266cef61b8e19c634de8d89e81860c062fa57bf8c85f934f6c4770c68c08",
+                "bytes": 838995968},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
                "sha256": "e432450e2f7a2466701f7b88d0a845213a66cc25fb0f8a12b0e26b1417e5df1c",
                "bytes": 584773632},
