@@ -42,6 +42,20 @@ def test_prefill_ragged_self_attention(cuda_lib):
     _check_all(cuda_lib, _batch(21, [200, 77, 1, 16, 33, 300]), "ragged causal")
 
 
+def test_prefill_empty_segment_and_loose_max_q_len(cuda_lib):
+    """A sequence with no new tokens between two that have some (its KV prefix is
+    never read), and max_q_len given as a loose upper bound: the grid then holds
+    work tiles past every sequence's end, which must do nothing."""
+    batch = _batch(23, [40, 0, 25], prefix=[0, 100, 50])
+    db = DeviceBatch(batch)
+    out, lse = cuda_lib.prefill(db.q, db.k, db.v, db.cu, db.kv_lens, db.bt, db.sinks,
+                                max_q_len=batch.max_q_len + 200, scale=batch.scale,
+                                causal=True, err_flag=db.err)
+    ref, ref_lse, _ = oracle_problem(batch).attention()
+    compare(out, lse, ref, ref_lse, what="empty segment")
+    assert db.err.item() == 0, db.err.item()
+
+
 def test_prefill_with_prefix(cuda_lib):
     """Chunked prefill: new tokens appended to an existing KV prefix (bottom-right causal)."""
     _check_all(cuda_lib, _batch(22, [64, 100, 5, 130], prefix=[0, 300, 17, 1000]), "prefix")
