@@ -18,7 +18,7 @@ import os
 import torch
 
 __all__ = ["load", "prefill", "decode", "merge", "decode_workspace_size", "status_string",
-           "AttnSinkError", "LIB_PATH", "FLAG_BAD_PAGE", "FLAG_TIMEOUT"]
+           "set_wait_limit_ns", "AttnSinkError", "LIB_PATH", "FLAG_BAD_PAGE", "FLAG_TIMEOUT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn_sink.so")
@@ -40,6 +40,7 @@ SIGNATURES = {
                                         [_f32, _i32, _i32, _vp, _vp], _i32),
     "attn_sink_merge": ([_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp], _i32),
     "attn_sink_status_string": ([_i32], ctypes.c_char_p),
+    "attn_sink_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_uint64),
 }
 
 
@@ -69,6 +70,12 @@ def load(path=None):
 
 def status_string(status):
     return load().attn_sink_status_string(int(status)).decode()
+
+
+def set_wait_limit_ns(ns):
+    """Test hook: limit of every pipeline wait for later calls (0 restores 1 s).
+    Returns the previous limit."""
+    return int(load().attn_sink_set_wait_limit_ns(int(ns)))
 
 
 def _check(fn, status):

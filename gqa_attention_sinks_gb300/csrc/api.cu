@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -17,6 +18,9 @@ namespace {
 
 constexpr int kGb300Sms = 152;  // split heuristic assumes the GB300 SM count
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Limit of each pipeline wait inside the kernels, read when a call is enqueued.
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -152,6 +156,10 @@ size_t partial_bytes(long long rows, int s_stride, size_t* o_bytes) {
 }  // namespace
 
 extern "C" {
+
+ATTN_SINK_API uint64_t attn_sink_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? kWaitLimitNs : ns);
+}
 
 ATTN_SINK_API const char* attn_sink_status_string(attn_sink_status status) {
   switch (status) {
@@ -297,6 +305,7 @@ attn_sink_status decode_impl(
   a.chunk_units = p.chunk_units;
   a.max_chunks = p.max_chunks;
   a.s_stride = p.s_stride;
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   a.k_new = k_new;
   a.v_new = v_new;
   a.k_cache_w = k_new ? const_cast<void*>(k_cache) : nullptr;
@@ -441,6 +450,7 @@ ATTN_SINK_API attn_sink_status attn_sink_prefill(
   a.num_pages = num_pages;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal;
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   return from_cuda(launch_prefill_bf16(a, q_map, k_map, v_map, s));
 }
 

@@ -200,7 +200,8 @@ __device__ __forceinline__ void consume_unit(uint32_t k_base, uint32_t v_base, i
   }
 }
 
-template <bool kTwoRows>
+// kPoll: the waits poll (a test's short wait limit); otherwise they block.
+template <bool kTwoRows, bool kPoll>
 __global__ void __launch_bounds__(kThreads)
     decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                         const __grid_constant__ CUtensorMap v_map, const DecodeArgs a) {
@@ -308,8 +309,8 @@ __global__ void __launch_bounds__(kThreads)
       }
       const int stage = it % kStages;
       if (it >= kStages) {
-        const bool ready = mbar_wait(&bars->empty[stage], ((it / kStages) + 1) & 1,
-                                     &bars->abort_word, a.err_flag);
+        const bool ready = mbar_wait<kPoll>(&bars->empty[stage], ((it / kStages) + 1) & 1,
+                                     &bars->abort_word, a.err_flag, a.wait_limit_ns);
         if (!__all_sync(0xffffffffu, ready)) break;
       }
       const int phys = __shfl_sync(0xffffffffu, cur_phys, it & 31);
@@ -375,7 +376,8 @@ __global__ void __launch_bounds__(kThreads)
 
   for (int it = 0; it < n_iters; ++it) {
     const int stage = it % kStages;
-    const bool ready = mbar_wait(&bars->full[stage], (it / kStages) & 1, &bars->abort_word, a.err_flag);
+    const bool ready =
+        mbar_wait<kPoll>(&bars->full[stage], (it / kStages) & 1, &bars->abort_word, a.err_flag, a.wait_limit_ns);
     if (!__all_sync(0xffffffffu, ready)) break;
     if (head_ok && bars->unit_ok[stage]) {
       const int u = u0 + it;
@@ -433,17 +435,12 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& k_map,
                                const CUtensorMap& v_map, cudaStream_t stream) {
   dim3 grid(a.max_chunks, (a.Hkv + kHeadsPerCta - 1) / kHeadsPerCta, a.B);
-  if (a.group > 8) {
-    auto kern = decode_split_kernel<true>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(k_map, v_map, a);
-  } else {
-    auto kern = decode_split_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(k_map, v_map, a);
-  }
+  const bool poll = a.wait_limit_ns < kPollLimitNs;
+  auto kern = a.group > 8 ? (poll ? decode_split_kernel<true, true> : decode_split_kernel<true, false>)
+                          : (poll ? decode_split_kernel<false, true> : decode_split_kernel<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(k_map, v_map, a);
   return cudaGetLastError();
 }
 

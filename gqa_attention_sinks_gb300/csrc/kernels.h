@@ -11,6 +11,11 @@ namespace attn_sink {
 constexpr int kHeadDim = 64;     // the only head dimension the kernels are built for
 constexpr int kUnitTokens = 16;  // keys per TMA box: one 16-row slice of a page
 constexpr int kHeadsPerCta = 4;  // decode: KV heads per CTA (one TMA box covers them)
+// Default limit of a pipeline wait inside the kernels, and the fixed limit of
+// the drains that let in-flight copies land before a CTA exits.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+// Limits below this (a test setting) run the kernels' polling instantiation.
+constexpr uint64_t kPollLimitNs = 1000000ull;  // 1 ms
 
 // ------------------------------------------------------------- bf16 decode
 struct DecodeArgs {
@@ -30,6 +35,7 @@ struct DecodeArgs {
   int chunk_units;             // 16-key units per chunk when num_splits == 0
   int max_chunks;              // grid.x
   int s_stride;                // partial slots per row in o_part / lse_part
+  uint64_t wait_limit_ns;      // limit of each pipeline wait (drains keep kWaitLimitNs)
   // Append mode (all null otherwise): before its keys are read, the step's
   // k_new / v_new [B, Hkv, 64] go into the slot of position kv_len - 1.
   const void* k_new;
@@ -110,6 +116,7 @@ struct PrefillArgs {
   int bt_stride, page_size, num_pages;
   float scale_log2;
   int causal;
+  uint64_t wait_limit_ns;      // limit of each pipeline wait (drains keep kWaitLimitNs)
 };
 
 cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,

@@ -166,6 +166,8 @@ __device__ __forceinline__ bool decode_tile(const PrefillArgs& a, const Meta& m,
   return true;
 }
 
+// kPoll: the waits poll (a test's short wait limit); otherwise they block.
+template <bool kPoll>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) {
         const int qb = qw % kQBufs;
         if (qw >= kQBufs) {
-          const bool ready = mbar_wait(&bars->q_empty[qb], ((qw / kQBufs) + 1) & 1, abort_word, a.err_flag);
+          const bool ready = mbar_wait<kPoll>(&bars->q_empty[qb], ((qw / kQBufs) + 1) & 1, abort_word, a.err_flag, a.wait_limit_ns);
           ok = __all_sync(0xffffffffu, ready);
           if (!ok) break;
         }
@@ -270,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         next_phys = entry_of(j + 1);
         const int st = kv_it % kStages;
         if (kv_it >= kStages) {
-          const bool ready = mbar_wait(&bars->kv_empty[st], ((kv_it / kStages) + 1) & 1, abort_word,
-                                       a.err_flag);
+          const bool ready = mbar_wait<kPoll>(&bars->kv_empty[st], ((kv_it / kStages) + 1) & 1, abort_word,
+                                       a.err_flag, a.wait_limit_ns);
           ok = __all_sync(0xffffffffu, ready);
           if (!ok) break;
         }
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_word, a.err_flag));
+      return __all_sync(0xffffffffu, mbar_wait<kPoll>(bar, parity, abort_word, a.err_flag, a.wait_limit_ns));
     };
     int qw = 0, kv_it = 0, it = 0, ow = 0;
     bool ok = true;
@@ -423,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = cur % kStages;
         // s_full completes after the MMA warp saw the stage's kv_full: the
         // stage has landed, and s_uok holds its unit mask.
-        const bool ready = mbar_wait(&bars->s_full[q], u & 1, abort_word, a.err_flag);
+        const bool ready = mbar_wait<kPoll>(&bars->s_full[q], u & 1, abort_word, a.err_flag, a.wait_limit_ns);
         ok = __all_sync(0xffffffffu, ready);
         if (!ok) break;
         const uint32_t uok = bars->s_uok[q];
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t negm2 = f2_pack(neg_m, neg_m);
         uint64_t ex2[4] = {0ull, 0ull, 0ull, 0ull};
         if (kQTiles > 1) {
-          const bool turn = mbar_wait(&bars->exp_turn[q], u & 1, abort_word, a.err_flag);
+          const bool turn = mbar_wait<kPoll>(&bars->exp_turn[q], u & 1, abort_word, a.err_flag, a.wait_limit_ns);
           ok = __all_sync(0xffffffffu, turn);
           if (!ok) break;
         }
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u > 0) {
           // The previous P*V must have consumed P (and updated O) before this P
           // and any rescale of O go into TMEM.
-          const bool done = mbar_wait(&bars->pv_done[q], (u - 1) & 1, abort_word, a.err_flag);
+          const bool done = mbar_wait<kPoll>(&bars->pv_done[q], (u - 1) & 1, abort_word, a.err_flag, a.wait_limit_ns);
           ok = __all_sync(0xffffffffu, done);
           if (!ok) break;
           tc_fence_after_sync();
@@ -582,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -------------------------------------------------------------- epilogue
       uint32_t o[2][32];
       if (w.n_kv > 0) {
-        const bool ready = mbar_wait(&bars->pv_done[q], (it + w.n_kv - 1) & 1, abort_word, a.err_flag);
+        const bool ready = mbar_wait<kPoll>(&bars->pv_done[q], (it + w.n_kv - 1) & 1, abort_word, a.err_flag, a.wait_limit_ns);
         ok = __all_sync(0xffffffffu, ready);
         if (!ok) break;
         tc_fence_after_sync();
@@ -656,17 +658,18 @@ cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kern = a.wait_limit_ns < kPollLimitNs ? prefill_kernel<true> : prefill_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split inside the kernel assumes the launch allocation; a
   // build that launched with fewer registers would make setmaxnreg.inc wait
   // for ever, so it is refused here instead.
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, prefill_kernel);
+  e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   const unsigned grid = static_cast<unsigned>(n_tiles < sms ? n_tiles : sms);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, a, n_tiles);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, a, n_tiles);
   return cudaGetLastError();
 }
 

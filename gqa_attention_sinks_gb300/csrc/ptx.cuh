@@ -2,8 +2,9 @@
 // TMA tile loads, bounded waits and small math helpers.
 //
 // Every wait in this library is bounded by wall-clock time (%globaltimer):
-// a wait that exceeds kWaitLimitNs sets the CTA's abort word and the
-// ATTN_SINK_FLAG_TIMEOUT bit, and returns false so the caller can unwind.
+// a pipeline wait that exceeds its limit (kWaitLimitNs unless a test lowered
+// it) sets the CTA's abort word and the ATTN_SINK_FLAG_TIMEOUT bit, and
+// returns false so the caller can unwind; drains always allow kWaitLimitNs.
 // Nothing here traps.
 #pragma once
 
@@ -12,11 +13,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kernels.h"
+
 namespace attn_sink {
 
 constexpr int kFlagBadPage = 1;
 constexpr int kFlagTimeout = 2;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
@@ -60,18 +62,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking check of the phase with the given parity (acquire on success).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false when
-// the CTA was told to abort or the wait ran past kWaitLimitNs (then it also
-// raises the abort word and the timeout flag).
+// the CTA was told to abort or the wait ran past limit_ns (then it also raises
+// the abort word and the timeout flag).  kPoll polls with test_wait instead
+// of try_wait: try_wait may hold the warp until the phase completes, so a
+// limit shorter than that hold (kPollLimitNs, a test setting) is only
+// enforced by polling.  Kernels are instantiated for both; a runtime choice
+// inside the wait loop measured 12 % slower in prefill.
+template <bool kPoll>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_word,
-                                          int* err_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                          int* err_flag, uint64_t limit_ns) {
+  if (kPoll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (kPoll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (*abort_word) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_word = 1;
         if (err_flag) atomicOr(err_flag, kFlagTimeout);
         return false;
@@ -81,7 +101,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // Waits for a phase regardless of the abort word (used to drain copies that
-// are still in flight before a CTA exits).  Bounded by kWaitLimitNs.
+// are still in flight before a CTA exits).  Always bounded by kWaitLimitNs,
+// whatever limit the pipeline waits use, so a copy has landed when it gives up.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();

@@ -220,6 +220,19 @@ ATTN_SINK_API attn_sink_status attn_sink_decode_static_scratch(
 /* Static description of a status code. */
 ATTN_SINK_API const char* attn_sink_status_string(attn_sink_status status);
 
+/*
+ * Test hook for the failure path.  Every pipeline wait inside the kernels
+ * (on a barrier that a copy, an MMA or another warp completes) gives up after
+ * a time limit: the CTA then sets ATTN_SINK_FLAG_TIMEOUT in err_flag, stops
+ * its pipeline, lets the copies it issued land (those drains always allow
+ * 1 s) and returns, so the CUDA context stays usable; that call's outputs are
+ * undefined.  The limit is 1 s.  This sets it, in nanoseconds, for calls
+ * enqueued afterwards by any thread of the process (0 restores 1 s), and
+ * returns the previous value.  A tiny limit makes a correct call time out,
+ * which is how the timeout path is tested without a fault.
+ */
+ATTN_SINK_API uint64_t attn_sink_set_wait_limit_ns(uint64_t ns);
+
 #ifdef __cplusplus
 }
 #endif

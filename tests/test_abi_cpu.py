@@ -39,6 +39,20 @@ def test_binding_signatures_cover_header():
     assert sorted(gas.SIGNATURES) == _declared()
 
 
+def test_wait_limit_hook_is_host_only(lib):
+    """The test hook for the timeout path only stores a value: it returns the
+    previous limit, and 0 restores the default of one second."""
+    f = lib.attn_sink_set_wait_limit_ns
+    f.argtypes = [ctypes.c_uint64]
+    f.restype = ctypes.c_uint64
+    first = f(12345)
+    try:
+        assert f(0) == 12345
+        assert f(0) == 1_000_000_000
+    finally:
+        f(first)
+
+
 def test_status_strings(lib):
     f = lib.attn_sink_status_string
     f.restype = ctypes.c_char_p
