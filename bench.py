@@ -43,11 +43,11 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "409f266cef61b8e19c634de8d89e81860c062fa57bf8c85f934f6c4770c68c08",
-                "bytes": 838995968},
+                "sha256": "96b03f70ffcad29fbf34294f4c7dabfb5e4d73de812638dc9aca62aad14cadc3",
+                "bytes": 740526592},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
-               "sha256": "e432450e2f7a2466701f7b88d0a845213a66cc25fb0f8a12b0e26b1417e5df1c",
-               "bytes": 584773632},
+               "sha256": "93a6febdfb38db5201f1340b73e0e6e973c36d5a3553235e5d235a66835c3eb0",
+               "bytes": 583148800},
 }
 
 
