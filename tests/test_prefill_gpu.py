@@ -203,3 +203,20 @@ def test_prefill_mixed_part_full(cuda_lib):
     ref, ref_lse, _ = oracle_problem(batch).attention(rows)
     compare(out, lse, ref, ref_lse, rows=rows, what="mixed prefill")
     assert db.err.item() == 0
+
+
+def test_prefill_mixed_batch_as_one_launch(cuda_lib):
+    """The whole mixed batch (48 decode sequences as one-token segments at their
+    last position, then four 512-token chunks over long prefixes, 1% outlier
+    keys) as a single prefill launch from one work list: every decode row and a
+    sample of the chunk rows against the oracle."""
+    batch = W.mixed_batch()["single"]
+    db = DeviceBatch(batch)
+    out, lse = _prefill(cuda_lib, db)
+    n_dec = batch.meta["n_decode"]
+    rows = np.unique(np.concatenate([np.arange(n_dec * batch.Hq),
+                                     W.sample_rows(np.random.default_rng(41), batch, 400)]))
+    ref, ref_lse, _ = oracle_problem(batch).attention(rows)
+    compare(out, lse, ref, ref_lse, rows=rows, what="mixed batch as one launch")
+    assert db.err.item() == 0, db.err.item()
+

@@ -270,7 +270,8 @@ def mixed_batch(seed=20260005, n_decode=48, decode_kv=(1024, 32768), n_prefill=4
     """Decode sequences plus chunked-prefill segments sharing one page pool.
 
     1% of (token, kv-head) K rows are scaled by 20 before rounding (outlier
-    logits).  Returns dict(decode=Batch, prefill=Batch).
+    logits).  Returns dict(decode=Batch, prefill=Batch, single=Batch), the last
+    being both parts as one ragged batch (decode sequences as 1-token segments).
     """
     rng = np.random.default_rng(seed)
     kv_dec = rng.integers(decode_kv[0], decode_kv[1] + 1, n_decode)
@@ -285,7 +286,14 @@ def mixed_batch(seed=20260005, n_decode=48, decode_kv=(1024, 32768), n_prefill=4
     prf = batch_from_pool(pool, np.arange(n_decode, n_decode + n_prefill),
                           np.full(n_prefill, prefill_new), qp, sinks, True, dtype,
                           dict(workload="mixed batch: chunked-prefill part", prefix=pre))
-    return dict(decode=dec, prefill=prf)
+    # The whole batch as one ragged query batch: each decode sequence is a
+    # one-token segment at its last position, then the chunked-prefill segments.
+    one = batch_from_pool(pool, np.arange(n_decode + n_prefill),
+                          np.concatenate([np.ones(n_decode, np.int64),
+                                          np.full(n_prefill, prefill_new, np.int64)]),
+                          np.concatenate([qd, qp]), sinks, True, dtype,
+                          dict(workload="mixed batch as one ragged batch", n_decode=n_decode))
+    return dict(decode=dec, prefill=prf, single=one)
 
 
 def sample_rows(rng, batch, n):
