@@ -430,12 +430,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const uint32_t uok = bars->s_uok[q];
         tc_fence_after_sync();
+        // S comes out of TMEM with its per-row maximum over each 32 columns
+        // (tcgen05.ld.red), so a tile whose keys are all visible needs no max
+        // arithmetic of its own.
         uint32_t s[4][32];
+        float cmax[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_taddr + 32 * c, s[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32_max(s_taddr + 32 * c, s[c], cmax[c]);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_tie(s[c]);
+        for (int c = 0; c < 4; ++c) {
+          tmem_tie(s[c]);
+          asm volatile("" : "+f"(cmax[c]));
+        }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free[q]);  // the MMA may now write the next S
@@ -458,10 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
           }
         }
+        float mx = fmaxf(max3f(cmax[0], cmax[1], cmax[2]), cmax[3]);
         if (!full) {
-          // Valid columns form a prefix [0, lim): keys below kv_len and, when
-          // causal, not after the row's position.  Skipped pages (rare) are
-          // cleared unit by unit.
+          // Some columns are not visible, and the maxima that came with S
+          // include them: mask, then take the row max here.  Valid columns
+          // form a prefix [0, lim): keys below kv_len and, when causal, not
+          // after the row's position.  Skipped pages (rare) are cleared unit
+          // by unit.
           int lim = w.kv_len - key_base;
           if (a.causal) lim = min(lim, static_cast<int>(pos - key_base + 1));
 #pragma unroll
@@ -476,10 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 32; ++i)
                 if (!((uok >> ((32 * c + i) / kUnitTokens)) & 1u)) s[c][i] = __float_as_uint(-INFINITY);
           }
-        }
-        // Row max: eight independent chains of 3-input max.
-        float mx;
-        {
+          // Row max: eight independent chains of 3-input max.
           float ch[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
