@@ -43,8 +43,8 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "96b03f70ffcad29fbf34294f4c7dabfb5e4d73de812638dc9aca62aad14cadc3",
-                "bytes": 740526592},
+                "sha256": "899f6ba5f5dcac4c6124f148b5e9b210ab236fcbaae9921da4c6f62aafa89cc5",
+                "bytes": 812987136},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
                "sha256": "93a6febdfb38db5201f1340b73e0e6e973c36d5a3553235e5d235a66835c3eb0",
                "bytes": 583148800},
