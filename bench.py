@@ -43,7 +43,7 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "899f6ba5f5dcac4c6124f148b5e9b210ab236fcbaae9921da4c6f62aafa89cc5",
+                "sha256": "c2483564f2c201150e0178281c7a0e3246294e7fc083421ddac7ded717e8e7bd",
                 "bytes": 812987136},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
                "sha256": "93a6febdfb38db5201f1340b73e0e6e973c36d5a3553235e5d235a66835c3eb0",

@@ -17,10 +17,11 @@
 //
 // Warp roles (384 threads):
 //   warps 0-3  softmax for Q tile 0, warps 4-7 softmax for Q tile 1: one
-//              thread per row; S comes out of TMEM with tcgen05.ld, the row
-//              max/exp2/sum run in registers, P (bf16) goes back into TMEM in
-//              its own columns and feeds P*V as the A operand.  The two
-//              warpgroups take turns in the exponential loop.
+//              thread per row; S comes out of TMEM with tcgen05.ld.red, which
+//              also returns the row's maximum, exp2 and the sum run in
+//              registers, P (bf16) goes back into TMEM in its own columns and
+//              feeds P*V as the A operand.  The two warpgroups take turns in
+//              the exponential loop.
 //   warp 8     TMA producer of Q and K: per work tile the two Q tiles
 //              (double-buffered), then per 128-key tile eight 16-row page
 //              slices of K into a 4-stage ring.  It runs ahead across work
