@@ -43,10 +43,10 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "exp2_poly.cuh", "kernels.h")],
-                "sha256": "c2483564f2c201150e0178281c7a0e3246294e7fc083421ddac7ded717e8e7bd",
+                "sha256": "78c8244eec28bb38175d335bca1f4cf8fba4d82f72883e9421ff3d381b62a7c1",
                 "bytes": 812987136},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
-               "sha256": "93a6febdfb38db5201f1340b73e0e6e973c36d5a3553235e5d235a66835c3eb0",
+               "sha256": "bb0a99524c531ef95cb63a834ce534f3e6b7126f07678c6335e654ce193ce02a",
                "bytes": 583148800},
 }
 
