@@ -1,19 +1,24 @@
 """Benchmark: sink GQA attention on GB300 (decode HBM GB/s, prefill TFLOP/s).
 
-Default (N=1): one JSON line whose headline workload is gpt-oss-shaped paged
+Default (N=1): one JSON line.  Its headline workload is gpt-oss-shaped paged
 decode (64 seqs, Hq 64, Hkv 8, D 64, KV lengths uniform in [512, 8192], page
 size 16, bf16).  A step is one decode call: the split-KV kernel plus the LSE
-merge, through the C ABI.  value = algorithmic K/V bytes per step / device
-time per step.  The prefill workload (8 x 4096 causal, ragged layout) is timed
-the same way and reported under "prefill" in TFLOP/s of the causal half.
+merge, through the C ABI; value = algorithmic K/V bytes per step / device
+time per step.  The other workloads are timed the same way and reported as
+sub-objects, each with its own roofline and CPU-oracle baseline:
+  "prefill"  8 x 4096 causal prefill, ragged layout (TFLOP/s of the causal half)
+  "long"     4 x 131072-key decode split into 32 chunks (GB/s)
+  "mixed"    48 decode seqs (KV 1k..32k) + 4 x 512-token chunked prefills over
+             prefixes up to 16k, 1% outlier keys: the decode part (GB/s) and the
+             chunked-prefill part (TFLOP/s), each against its own roofline
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|prefill|long|mixed] [--no-cpu-baseline]
+                    [--workload all|decode|prefill|long|mixed] [--no-cpu-baseline]
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload with a
 rank-specific seed (weak scaling, no collective on the data path); timing is
 the max over ranks.  --impl reference times the fp64 CPU oracle on the host
-cores over a bounded sample of the same workload.
+cores over a bounded sample of the headline workload.
 """
 import argparse
 import json
@@ -36,18 +41,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
-# dominant kernel, from the ncu captures summarised in profiles/.  A value holds
-# only for the kernel sources it was captured with (sha256 over the listed files);
-# after any change to them the roofline reports traffic = null.
+# dominant kernel of a workload, from the ncu captures summarised in profiles/.  A
+# value holds only for the kernel sources it was captured with (sha256 over the
+# listed files); after any change to them the roofline reports traffic = null.
 CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
-                                               "exp2_poly.cuh", "kernels.h")],
-                "sha256": "78c8244eec28bb38175d335bca1f4cf8fba4d82f72883e9421ff3d381b62a7c1",
-                "bytes": 812987136},
+                                               "kernels.h")],
+                "sha256": "", "bytes": None},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
-               "sha256": "bb0a99524c531ef95cb63a834ce534f3e6b7126f07678c6335e654ce193ce02a",
-               "bytes": 583148800},
+               "sha256": "", "bytes": None},
 }
 
 
@@ -93,15 +96,62 @@ def decode_bytes(batch):
     return kv + io + pages
 
 
-def prefill_flops(batch):
-    """Algorithmic FLOPs of causal prefill: 4*D per visible (query row, key) pair."""
+def visible_pairs(batch, rows=None):
+    """(query row, key) pairs the rows see (all rows of the batch when rows is None)."""
     q = batch.q_lens.astype(np.int64)
     kv = batch.kv_lens.astype(np.int64)
-    pairs = 0
-    for ql, kl in zip(q, kv):
-        first = kl - ql + 1                       # keys seen by the first query
-        pairs += ql * first + ql * (ql - 1) // 2 if batch.causal else ql * kl
-    return 4 * batch.D * batch.Hq * int(pairs)
+    if rows is None:
+        pairs = 0
+        for ql, kl in zip(q, kv):
+            if batch.causal:
+                first = kl - ql + 1                   # keys seen by the first query
+                pairs += ql * first + ql * (ql - 1) // 2
+            else:
+                pairs += ql * kl
+        return int(pairs) * batch.Hq
+    tok = np.asarray(rows, np.int64) // batch.Hq
+    seq = np.searchsorted(batch.cu_seqlens_q, tok, side="right") - 1
+    i = tok - batch.cu_seqlens_q[seq]
+    pos = kv[seq] - q[seq] + i
+    seen = np.clip(pos + 1, 0, kv[seq]) if batch.causal else kv[seq]
+    return int(seen.sum())
+
+
+def prefill_flops(batch):
+    """Algorithmic FLOPs of causal prefill: 4*D per visible (query row, key) pair."""
+    return 4 * batch.D * visible_pairs(batch)
+
+
+def time_region(fn, steps, warmup, *, sync, barrier, reduce_max, clock):
+    """Runs `warmup` untimed steps, then times exactly `steps` steps bracketed by
+    sync + barrier + sync on both sides; returns the maximum over ranks (ms).
+    clock() returns (start, stop) callables; stop(start_token) gives ms."""
+    for _ in range(warmup):
+        fn()
+    sync()
+    barrier()
+    sync()
+    start, stop = clock()
+    tok = start()
+    for _ in range(steps):
+        fn()
+    ms = stop(tok)
+    sync()
+    barrier()
+    return reduce_max(ms)
+
+
+def make_reduce_max(ws, device):
+    """Max of a float over the ranks of the default process group (identity at N=1)."""
+    def reduce_max(x):
+        if ws == 1:
+            return float(x)
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return reduce_max
 
 
 class ClockSampler:
@@ -153,126 +203,224 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
+# ----------------------------------------------------------------- CPU oracle
+def cpu_oracle_rate(batch, seconds, unit, rng_seed=7):
+    """Time the fp64 oracle on the host cores over a bounded sample of the batch.
+
+    Decode-like batches (one query per sequence) are sampled by whole sequences,
+    in order, and rated in GB/s of algorithmic K/V bytes; prefill batches by
+    random query tokens (all heads) in groups of 64, rated in TFLOP/s of the
+    algorithmic 4*D FLOPs per visible (row, key) pair.  Runs about `seconds`."""
+    import oracle
+    prob = oracle.Problem(batch.q, batch.k_cache, batch.v_cache, batch.cu_seqlens_q,
+                          batch.kv_lens, batch.block_table, batch.sinks, batch.scale, batch.causal)
+    rng = np.random.default_rng(rng_seed)
+    work, elapsed, units = 0, 0.0, 0
+    b = 0
+    while elapsed < seconds and units < 100000:
+        if unit == "GB/s":
+            rows = np.arange(batch.cu_seqlens_q[b] * batch.Hq, batch.cu_seqlens_q[b + 1] * batch.Hq)
+            w = visible_pairs(batch, rows) * batch.D * 2 * 2 // (batch.Hq // batch.Hkv)
+            b = (b + 1) % batch.B
+            units += 1
+        else:
+            toks = rng.choice(batch.total_q, size=min(64, batch.total_q), replace=False)
+            rows = (toks[:, None] * batch.Hq + np.arange(batch.Hq)[None, :]).reshape(-1)
+            w = 4 * batch.D * visible_pairs(batch, rows)
+            units += len(toks)
+        t0 = time.perf_counter()
+        prob.attention(rows)
+        elapsed += time.perf_counter() - t0
+        work += w
+    value = work / elapsed / (1e9 if unit == "GB/s" else 1e12)
+    what = ("%d whole sequences (all heads)" % units if unit == "GB/s"
+            else "%d random query tokens (all heads)" % units)
+    return {"value": round(value, 4), "unit": unit, "cores": oracle.max_threads(),
+            "kind": "oracle", "sample": "%s, %.1f s of fp64 oracle time" % (what, elapsed)}
+
+
 # ----------------------------------------------------------------- GPU arm
-def run_ours(args, ws, rank, local):
-    import torch
-    import gqa_attention_sinks_gb300 as gas
+class GpuArm:
+    def __init__(self, args, ws, rank, local):
+        import torch
+        import gqa_attention_sinks_gb300 as gas
+        self.torch, self.gas = torch, gas
+        self.args, self.ws, self.rank, self.local = args, ws, rank, local
+        torch.cuda.set_device(local)
+        gas.load()
+        self.dev = torch.device("cuda", local)
+        self.stream = torch.cuda.current_stream()
+        self.pk, self.pk_kind = peaks()
+        self.reduce_max = make_reduce_max(ws, self.dev)
+        self.seed_off = 1000 * rank
 
-    torch.cuda.set_device(local)
-    gas.load()
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    pk, pk_kind = peaks()
-
-    def to_dev(a):
+    # -- plumbing
+    def to_dev(self, a):
+        torch = self.torch
         if a.dtype == np.uint16:
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(self.dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
 
-    def pinned(a):
+    def pinned(self, a):
+        torch = self.torch
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
                              else np.ascontiguousarray(a))
         t = t.pin_memory()
         return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
 
-    def barrier():
-        if ws > 1:
-            torch.distributed.barrier()
+    def barrier(self):
+        if self.ws > 1:
+            self.torch.distributed.barrier()
 
-    def max_over_ranks(x):
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+    def event_clock(self):
+        torch, stream = self.torch, self.stream
 
-    def timed(fn, steps, warmup, per_call=False):
-        """Device time of `steps` calls after `warmup` calls (ms total, per-call list)."""
-        for _ in range(warmup):
+        def start():
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            return e
+
+        def stop(e0):
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+        return start, stop
+
+    def timed(self, fn, steps, warmup):
+        """Total ms of `steps` back-to-back calls (max over ranks)."""
+        return time_region(fn, steps, warmup, sync=self.torch.cuda.synchronize,
+                           barrier=self.barrier, reduce_max=self.reduce_max,
+                           clock=self.event_clock)
+
+    def per_call(self, fn, steps):
+        """Mean device time of one call, each call bracketed by its own events."""
+        torch, stream = self.torch, self.stream
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            a.record(stream)
             fn()
+            b.record(stream)
         torch.cuda.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        per = []
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        if per_call:
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(steps)]
-        t0.record(stream)
-        for i in range(steps):
-            if per_call:
-                evs[i][0].record(stream)
+        return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+    def with_clocks(self, run):
+        sampler = ClockSampler(self.local)
+        sampler.start()
+        try:
+            out = run()
+        finally:
+            clocks = sampler.stop()
+        return out, clocks
+
+    def warm_clock(self, fn):
+        t_end = time.time() + self.args.clock_window   # load the GPU while sampling starts
+        while time.time() < t_end:
             fn()
-            if per_call:
-                evs[i][1].record(stream)
-        t1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        total = t0.elapsed_time(t1)
-        if per_call:
-            per = [a.elapsed_time(b) for a, b in evs]
-        return max_over_ranks(total), per
+            self.torch.cuda.synchronize()
 
-    seed_off = 1000 * rank
-    result = {}
-
-    # ---------------------------------------------------------- decode
-    if args.workload in ("decode", "long", "mixed"):
-        if args.workload == "decode":
-            batch = W.gptoss_decode(seed=20260002 + seed_off)
-            splits = 0
-            wl = ("gpt-oss decode: 64 seqs, Hq 64, Hkv 8, D 64, KV lengths U[512, 8192], "
-                  "page 16, shuffled page table, bf16")
-        elif args.workload == "long":
-            batch = W.long_split_decode(seed=20260004 + seed_off)
-            splits = 32
-            wl = "long split-KV decode: 4 seqs x 131072 keys, 32 chunks, Hq 64, Hkv 8, D 64, bf16"
-        else:
-            batch = W.mixed_batch(seed=20260005 + seed_off)["decode"]
-            splits = 0
-            wl = "mixed batch, decode part: 48 seqs, KV U[1024, 32768], Hq 64, Hkv 8, bf16"
-        q, k, v = to_dev(batch.q), to_dev(batch.k_cache), to_dev(batch.v_cache)
-        kvl, bt, sinks = to_dev(batch.kv_lens), to_dev(batch.block_table), to_dev(batch.sinks)
-        out = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    # -- the calls
+    def decode_step(self, batch, splits):
+        torch, gas = self.torch, self.gas
+        d = dict(q=self.to_dev(batch.q), k=self.to_dev(batch.k_cache), v=self.to_dev(batch.v_cache),
+                 kvl=self.to_dev(batch.kv_lens), bt=self.to_dev(batch.block_table),
+                 sinks=self.to_dev(batch.sinks))
+        d["out"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=self.dev)
         need = gas.decode_workspace_size(batch.B, batch.Hq, batch.Hkv, batch.D,
                                          batch.block_table.shape[1], batch.page_size, splits)
-        wsbuf = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        d["ws"] = torch.empty(max(need, 256), dtype=torch.uint8, device=self.dev)
+        d["launches"] = 2 if need > 0 else 1
 
         def step():
-            gas.decode(q, k, v, kvl, bt, sinks, scale=batch.scale, num_splits=splits, out=out,
-                       lse=lse, workspace=wsbuf)
+            gas.decode(d["q"], d["k"], d["v"], d["kvl"], d["bt"], d["sinks"], scale=batch.scale,
+                       num_splits=splits, out=d["out"], lse=d["lse"], workspace=d["ws"])
+        return step, d
 
+    def prefill_step(self, batch):
+        torch, gas = self.torch, self.gas
+        d = dict(q=self.to_dev(batch.q), k=self.to_dev(batch.k_cache), v=self.to_dev(batch.v_cache),
+                 cu=self.to_dev(batch.cu_seqlens_q), kvl=self.to_dev(batch.kv_lens),
+                 bt=self.to_dev(batch.block_table), sinks=self.to_dev(batch.sinks))
+        d["out"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=self.dev)
+        need = gas.prefill_workspace_size(batch.B, batch.Hq, batch.D, batch.max_q_len)
+        d["ws"] = torch.empty(max(need, 256), dtype=torch.uint8, device=self.dev)
+
+        def step():
+            gas.prefill(d["q"], d["k"], d["v"], d["cu"], d["kvl"], d["bt"], d["sinks"],
+                        max_q_len=batch.max_q_len, scale=batch.scale, out=d["out"], lse=d["lse"],
+                        workspace=d["ws"])
+        return step, d
+
+    # -- parts
+    def hbm_roofline(self, nbytes, call_ms, traffic_kind, kernel):
+        ach = nbytes / (call_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": self.pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / self.pk["hbm_gbs"], 4),
+                "traffic": ncu_traffic(traffic_kind) if traffic_kind else None,
+                "peak_source": self.pk_kind, "kernel": kernel}
+
+    def tensor_roofline(self, flops, call_ms, traffic_kind):
+        ach = flops / (call_ms * 1e-3) / 1e12
+        peak = self.pk["bf16_tflops"]
+        return {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4),
+                "traffic": ncu_traffic(traffic_kind) if traffic_kind else None,
+                "peak_source": self.pk_kind, "kernel": "prefill_kernel (tcgen05, one launch)"}
+
+    def decode_part(self, batch, splits, name, steps, traffic_kind):
+        step, d = self.decode_step(batch, splits)
         nbytes = decode_bytes(batch)
-        sampler = ClockSampler(local)
-        sampler.start()
-        t_end = time.time() + args.clock_window
-        while time.time() < t_end:                 # clock window: load the GPU for sampling
-            step()
-            torch.cuda.synchronize()
-        total_ms, _ = timed(step, args.steps, args.warmup)
-        _, per = timed(step, args.steps, 0, per_call=True)
-        clocks = sampler.stop()
-        ms = total_ms / args.steps
-        call_ms = float(np.mean(per))
-        value = ws * nbytes / (ms * 1e-3) / 1e9
-        achieved = nbytes / (call_ms * 1e-3) / 1e9
-        launches_per_step = 2 if need > 0 else 1
 
-        # End to end through the C ABI: every step copies all its inputs from pinned
-        # host memory and reads its result back.  Two device input sets alternate, so
-        # the copy of step i+1 (on a copy stream) overlaps the decode of step i; the
-        # decode of a set waits for that set's copy, and a set is refilled only after
-        # the decode that read it has finished.
-        h_in = [pinned(a) for a in (batch.q, batch.k_cache, batch.v_cache, batch.kv_lens,
-                                    batch.block_table, batch.sinks)]
-        sets = [[q, k, v, kvl, bt, sinks], [torch.empty_like(t) for t in (q, k, v, kvl, bt, sinks)]]
-        outs = [(out, lse), (torch.empty_like(out), torch.empty_like(lse))]
-        wss = [wsbuf, torch.empty_like(wsbuf)]
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        copy_stream = torch.cuda.Stream(device=dev)
+        def run():
+            self.warm_clock(step)
+            total = self.timed(step, steps, self.args.warmup)
+            return total, self.per_call(step, steps)
+        (total_ms, call_ms), clocks = self.with_clocks(run)
+        ms = total_ms / steps
+        part = {"workload": name, "value": round(self.ws * nbytes / (ms * 1e-3) / 1e9, 1),
+                "unit": "GB/s", "ms_per_step": round(ms, 5), "steps": steps,
+                "num_splits": splits, "bytes_per_step": nbytes,
+                "roofline": self.hbm_roofline(nbytes, call_ms, traffic_kind,
+                                              "decode split kernel + LSE merge (one C-ABI call)"),
+                "gpu_launches": d["launches"] * steps, "clocks": clocks}
+        return part, step, d
+
+    def prefill_part(self, batch, name, steps, traffic_kind):
+        step, d = self.prefill_step(batch)
+        flops = prefill_flops(batch)
+
+        def run():
+            self.warm_clock(step)
+            total = self.timed(step, steps, self.args.warmup)
+            return total, self.per_call(step, steps)
+        (total_ms, call_ms), clocks = self.with_clocks(run)
+        ms = total_ms / steps
+        part = {"workload": name, "value": round(self.ws * flops / (ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(ms, 5), "steps": steps,
+                "flops_per_step": flops, "roofline": self.tensor_roofline(flops, call_ms, traffic_kind),
+                "gpu_launches": steps, "clocks": clocks}
+        return part, step
+
+    def e2e_decode(self, batch, splits, d):
+        """End to end through the C ABI: every step copies all its inputs from pinned
+        host memory and reads its result back.  Two device input sets alternate, so
+        the copy of step i+1 (on a copy stream) overlaps the decode of step i; the
+        decode of a set waits for that set's copy, and a set is refilled only after
+        the decode that read it has finished."""
+        torch, gas, stream = self.torch, self.gas, self.stream
+        h_in = [self.pinned(a) for a in (batch.q, batch.k_cache, batch.v_cache, batch.kv_lens,
+                                         batch.block_table, batch.sinks)]
+        first = [d["q"], d["k"], d["v"], d["kvl"], d["bt"], d["sinks"]]
+        sets = [first, [torch.empty_like(t) for t in first]]
+        outs = [(d["out"], d["lse"]), (torch.empty_like(d["out"]), torch.empty_like(d["lse"]))]
+        wss = [d["ws"], torch.empty_like(d["ws"])]
+        h_out = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
+        h_lse = torch.empty(d["lse"].shape, dtype=d["lse"].dtype).pin_memory()
+        copy_stream = torch.cuda.Stream(device=self.dev)
         copied = [torch.cuda.Event(), torch.cuda.Event()]
         freed = [torch.cuda.Event(), torch.cuda.Event()]
 
@@ -281,8 +429,8 @@ def run_ours(args, ws, rank, local):
             d_in, (o_d, l_d) = sets[st], outs[st]
             copy_stream.wait_event(freed[st])
             with torch.cuda.stream(copy_stream):
-                for h, d in zip(h_in, d_in):
-                    d.copy_(h, non_blocking=True)
+                for h, dv in zip(h_in, d_in):
+                    dv.copy_(h, non_blocking=True)
                 copied[st].record(copy_stream)
             stream.wait_event(copied[st])
             gas.decode(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], d_in[5], scale=batch.scale,
@@ -293,127 +441,128 @@ def run_ours(args, ws, rank, local):
 
         for st in range(2):                        # both sets' events exist before timing
             freed[st].record(stream)
-        e2e_steps = max(4, min(args.steps, 20))
+        steps = max(4, min(self.args.steps, 20))
         for i in range(2):                         # warm-up
             e2e_step(i)
         torch.cuda.synchronize()
-        barrier()
+        self.barrier()
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         copy_stream.wait_stream(stream)            # the first copy starts after t0
-        for i in range(e2e_steps):
+        for i in range(steps):
             e2e_step(i)
         t1.record(stream)                          # after the last decode and read-back
         torch.cuda.synchronize()
-        barrier()
-        e2e_ms = max_over_ranks(t0.elapsed_time(t1)) / e2e_steps
+        self.barrier()
+        ms = self.reduce_max(t0.elapsed_time(t1)) / steps
         h2d = sum(t.numel() * t.element_size() for t in h_in)
         d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+        nbytes = decode_bytes(batch)
+        return {"value": round(self.ws * nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h}
 
-        result = {
-            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded normal q/k/v, shuffled page table)",
-            "config": {"workload": wl, "num_splits": splits,
-                       "l2": "inputs larger than L2: %.0f MB of K/V per step" % (nbytes / 1e6),
-                       "bytes_per_step": nbytes},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
-                         "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / pk["hbm_gbs"], 4),
-                         "traffic": ncu_traffic("decode") if args.workload == "decode" else None,
-                         "peak_source": pk_kind,
-                         "kernel": "decode split kernel + LSE merge (one C-ABI call)"},
-            "e2e": {"value": round(ws * nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks,
-        }
+    def release(self, *objs):
+        for o in objs:
+            if isinstance(o, dict):
+                o.clear()
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
 
-    # ---------------------------------------------------------- prefill
-    if (args.workload in ("decode", "prefill", "mixed")) and not args.no_prefill:
-        if args.workload == "mixed":
-            pre = W.mixed_batch(seed=20260005 + seed_off)["prefill"]
-            pre_name = ("mixed batch, chunked-prefill part: 4 x 512 new tokens over prefixes "
-                        "U[0, 16384], Hq 64, Hkv 8, D 64, bf16, paged K/V, 1% outlier keys")
-        else:
-            pre = W.gptoss_prefill(seed=20260003 + seed_off)
-            pre_name = ("gpt-oss causal prefill: 8 seqs x 4096, Hq 64, Hkv 8, D 64, bf16, "
-                        "ragged cu_seqlens, paged K/V")
-        q, k, v = to_dev(pre.q), to_dev(pre.k_cache), to_dev(pre.v_cache)
-        cu, kvl = to_dev(pre.cu_seqlens_q), to_dev(pre.kv_lens)
-        bt, sinks = to_dev(pre.block_table), to_dev(pre.sinks)
-        out = torch.empty_like(q)
-        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
 
-        def pstep():
-            gas.prefill(q, k, v, cu, kvl, bt, sinks, max_q_len=pre.max_q_len, scale=pre.scale,
-                        out=out, lse=lse)
+def cpu_baselines_wanted(args, ws, rank):
+    return rank == 0 and ws == 1 and not args.no_cpu_baseline
 
-        flops = prefill_flops(pre)
-        part = {"workload": pre_name, "flops_per_step": flops}
-        try:
+
+def run_ours(args, ws, rank, local):
+    arm = GpuArm(args, ws, rank, local)
+    so = arm.seed_off
+    steps = args.steps
+    want_cpu = cpu_baselines_wanted(args, ws, rank)
+    sub = {}
+    head = None
+
+    if args.workload in ("all", "decode"):
+        batch = W.gptoss_decode(seed=20260002 + so)
+        name = ("gpt-oss decode: 64 seqs, Hq 64, Hkv 8, D 64, KV lengths U[512, 8192], page 16, "
+                "shuffled page table, bf16")
+        part, step, d = arm.decode_part(batch, 0, name, steps, "decode")
+        part["e2e"] = arm.e2e_decode(batch, 0, d)
+        if want_cpu:
+            part["cpu_baseline"] = cpu_oracle_rate(batch, args.cpu_seconds, "GB/s")
+        arm.release(d)
+        head = part
+
+    if args.workload in ("all", "prefill"):
+        batch = W.gptoss_prefill(seed=20260003 + so)
+        name = ("gpt-oss causal prefill: 8 seqs x 4096, Hq 64, Hkv 8, D 64, bf16, ragged "
+                "cu_seqlens, paged K/V, out bf16 + fp32 lse")
+        part, _ = arm.prefill_part(batch, name, max(3, min(steps, 50)), "prefill")
+        if want_cpu:
+            part["cpu_baseline"] = cpu_oracle_rate(batch, args.cpu_seconds, "TFLOP/s")
+        arm.release()
+        sub["prefill"] = part
+        del batch
+
+    if args.workload in ("all", "long"):
+        batch = W.long_split_decode(seed=20260004 + so)
+        name = "long split-KV decode: 4 seqs x 131072 keys, 32 chunks, Hq 64, Hkv 8, D 64, bf16"
+        part, _, d = arm.decode_part(batch, 32, name, max(3, min(steps, 100)), None)
+        if want_cpu:
+            part["cpu_baseline"] = cpu_oracle_rate(batch, args.cpu_seconds, "GB/s")
+        arm.release(d)
+        sub["long"] = part
+        del batch
+
+    if args.workload in ("all", "mixed"):
+        m = W.mixed_batch(seed=20260005 + so)
+        k = max(3, min(steps, 100))
+        dpart, dstep, d = arm.decode_part(
+            m["decode"], 0, "mixed batch, decode part: 48 seqs, KV U[1024, 32768], Hq 64, Hkv 8, "
+            "D 64, bf16, 1% outlier keys", k, None)
+        ppart, pstep = arm.prefill_part(
+            m["prefill"], "mixed batch, chunked-prefill part: 4 x 512 new tokens over prefixes "
+            "U[0, 16384], Hq 64, Hkv 8, D 64, bf16, 1% outlier keys", k, None)
+
+        def both():
+            dstep()
             pstep()
-            torch.cuda.synchronize()
-            psteps = max(3, min(args.steps, 50))
-            sampler = ClockSampler(local)
-            sampler.start()
-            t_end = time.time() + args.clock_window
-            while time.time() < t_end:
-                pstep()
-                torch.cuda.synchronize()
-            total_ms, per = timed(pstep, psteps, args.warmup, per_call=True)
-            pclocks = sampler.stop()
-            pms = total_ms / psteps
-            call_ms = float(np.mean(per))
-            ach = flops / (call_ms * 1e-3) / 1e12
-            peak = pk["bf16_tflops"]
-            part.update({"value": round(ws * flops / (pms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                         "ms_per_step": round(pms, 4), "steps": psteps, "clocks": pclocks,
-                         "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peak,
-                                      "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                                      "traffic": (ncu_traffic("prefill") if args.workload != "mixed"
-                                                  else None),
-                                      "peak_source": pk_kind}})
-        except gas.AttnSinkError as e:
-            part.update({"unavailable": str(e)})
-        if result:
-            result["prefill"] = part
-        else:
-            result = {"metric": METRIC, "value": part.get("value"), "unit": "TFLOP/s",
-                      "n_gpus": ws, "steps": part.get("steps", args.steps), "warmup": args.warmup,
-                      "ms_per_step": part.get("ms_per_step"), "higher_is_better": True,
-                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                      "data": "synthetic (seeded normal q/k/v)",
-                      "config": {"workload": part["workload"]},
-                      "roofline": part.get("roofline"), "gpu_launches": part.get("steps", 0),
-                      "clocks": part.get("clocks")}
-    return result
+        total = arm.timed(both, k, args.warmup)
+        if want_cpu:
+            dpart["cpu_baseline"] = cpu_oracle_rate(m["decode"], args.cpu_seconds / 2, "GB/s")
+            ppart["cpu_baseline"] = cpu_oracle_rate(m["prefill"], args.cpu_seconds / 2, "TFLOP/s")
+        arm.release(d)
+        sub["mixed"] = {"workload": "mixed batch: decode part then chunked-prefill part, two "
+                                    "launches on one stream",
+                        "ms_per_step": round(total / k, 5), "decode": dpart, "prefill": ppart}
+        del m
 
-
-# ----------------------------------------------------------------- CPU oracle
-def cpu_oracle_rate(batch, seconds, max_seqs=None, rows_per_seq=None):
-    """Time the fp64 oracle on the host cores over whole sequences of the batch.
-
-    Returns (GB/s of algorithmic K/V bytes, threads, sample description, steps)."""
-    import oracle
-    prob = oracle.Problem(batch.q, batch.k_cache, batch.v_cache, batch.cu_seqlens_q,
-                          batch.kv_lens, batch.block_table, batch.sinks, batch.scale, batch.causal)
-    n = batch.B if max_seqs is None else min(max_seqs, batch.B)
-    done_bytes, elapsed, seqs = 0, 0.0, 0
-    b = 0
-    while elapsed < seconds and seqs < 1000 * batch.B:  # about `seconds` of oracle work
-        rows = np.arange(batch.cu_seqlens_q[b] * batch.Hq, batch.cu_seqlens_q[b + 1] * batch.Hq)
-        t0 = time.perf_counter()
-        prob.attention(rows)
-        elapsed += time.perf_counter() - t0
-        done_bytes += int(batch.kv_lens[b]) * batch.Hkv * batch.D * 4
-        seqs += 1
-        b = (b + 1) % n
-    return done_bytes / elapsed / 1e9, oracle.max_threads(), "%d whole sequences" % seqs, elapsed
+    if head is None:
+        # a single non-headline workload: its own numbers head the line
+        key = next(iter(sub))
+        p = sub.pop(key)
+        if key == "mixed":
+            p = dict(p["decode"], mixed_prefill=p["prefill"], ms_both=p["ms_per_step"])
+        head = p
+    res = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": ws,
+           "steps": head["steps"], "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded normal q/k/v, shuffled page table)",
+           "config": {"workload": head["workload"],
+                      "l2": "inputs larger than L2 (129 MB): no flush between steps"},
+           "roofline": head["roofline"], "gpu_launches": head["gpu_launches"],
+           "clocks": head["clocks"]}
+    for k in ("e2e", "cpu_baseline", "num_splits", "bytes_per_step", "flops_per_step"):
+        if k in head:
+            (res["config"] if k in ("num_splits", "bytes_per_step", "flops_per_step")
+             else res)[k] = head[k]
+    for k, v in head.items():
+        if k in ("mixed_prefill", "ms_both"):
+            res[k] = v
+    res.update(sub)
+    return res
 
 
 def run_reference(args, ws, rank):
@@ -460,11 +609,12 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill", "long", "mixed"], default="decode")
+    ap.add_argument("--workload", choices=["all", "decode", "prefill", "long", "mixed"],
+                    default="all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--clock-window", type=float, default=2.0,
+    ap.add_argument("--cpu-seconds", type=float, default=6.0,
+                    help="seconds of fp64 oracle time per workload for the CPU baselines")
+    ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of untimed steps run while clock sampling starts")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -482,11 +632,6 @@ def main():
         res = run_reference(args, ws, rank)
     else:
         res = run_ours(args, ws, rank, local)
-        if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.workload in ("decode",):
-            batch = W.gptoss_decode()
-            rate, threads, sample, secs = cpu_oracle_rate(batch, args.cpu_seconds)
-            res["cpu_baseline"] = {"value": round(rate, 3), "unit": "GB/s", "cores": threads,
-                                   "kind": "oracle", "sample": sample + " (%.1f s)" % secs}
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()

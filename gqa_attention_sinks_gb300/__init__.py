@@ -17,7 +17,8 @@ import os
 
 import torch
 
-__all__ = ["load", "prefill", "decode", "merge", "decode_workspace_size", "status_string",
+__all__ = ["load", "prefill", "decode", "decode_append", "merge", "decode_workspace_size",
+           "prefill_workspace_size", "status_string",
            "set_wait_limit_ns", "AttnSinkError", "LIB_PATH", "FLAG_BAD_PAGE", "FLAG_TIMEOUT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +31,8 @@ _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c
 
 # C-ABI signatures (argument types, return type), mirroring include/attn_sink.h.
 SIGNATURES = {
-    "attn_sink_prefill": ([_vp] * 10 + [_i32] * 8 + [_f32, _i32, _i32, _vp, _vp], _i32),
+    "attn_sink_prefill": ([_vp] * 10 + [_i32] * 8 + [_f32, _i32, _i32, _vp, _vp, _sz, _vp], _i32),
+    "attn_sink_prefill_workspace_size": ([_i32] * 4, _sz),
     "attn_sink_decode": ([_vp] * 5 + [_i32, _vp, _vp, _vp] + [_i32] * 6 + [_f32, _i32, _i32, _vp,
                                                                          _vp, _sz, _vp], _i32),
     "attn_sink_decode_append": ([_vp] * 7 + [_i32, _vp, _vp, _vp] + [_i32] * 6 +
@@ -116,6 +118,11 @@ def decode_workspace_size(B, Hq, Hkv, D, block_table_stride, page_size, num_spli
                                                       page_size, num_splits))
 
 
+def prefill_workspace_size(B, Hq, D, max_q_len):
+    """Bytes of scratch ``prefill`` needs for these arguments."""
+    return int(load().attn_sink_prefill_workspace_size(B, Hq, D, max_q_len))
+
+
 def decode(q, k_cache, v_cache, kv_lens, block_table, sinks, *, scale=None, num_splits=0,
            out=None, lse=None, workspace=None, err_flag=None, stream=None):
     """Paged decode with sinks.  q [B, Hq, D]; caches [pages, page_size, Hkv, D].
@@ -190,12 +197,13 @@ def decode_append(q, k_new, v_new, k_cache, v_cache, kv_lens, block_table, sinks
     return out, lse
 
 
-def prefill(q, k_cache, v_cache, cu_seqlens_q, kv_lens, block_table, sinks, *, max_q_len=None,
-            scale=None, causal=True, out=None, lse=None, err_flag=None, stream=None):
+def prefill(q, k_cache, v_cache, cu_seqlens_q, kv_lens, block_table, sinks, *, max_q_len,
+            scale=None, causal=True, out=None, lse=None, workspace=None, err_flag=None,
+            stream=None):
     """Ragged causal prefill with sinks.  q [total_q, Hq, D].
 
-    max_q_len is a host int (an upper bound of every q_len); when omitted it is
-    read from cu_seqlens_q, which synchronises the stream.
+    max_q_len is a host int, an upper bound of every sequence's q_len (the
+    caller knows it; reading it from cu_seqlens_q would synchronise).
     Returns (out [total_q, Hq, D] in q's dtype, lse [total_q, Hq] fp32).
     """
     lib = load()
@@ -209,8 +217,6 @@ def prefill(q, k_cache, v_cache, cu_seqlens_q, kv_lens, block_table, sinks, *, m
     total_q, Hq, D = q.shape
     num_pages, page_size, Hkv, _ = k_cache.shape
     B = kv_lens.shape[0]
-    if max_q_len is None:
-        max_q_len = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
@@ -218,11 +224,15 @@ def prefill(q, k_cache, v_cache, cu_seqlens_q, kv_lens, block_table, sinks, *, m
         lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
     _dev(out, "out", q.dtype)
     _dev(lse, "lse", torch.float32)
+    need = prefill_workspace_size(B, Hq, D, int(max_q_len))
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib.attn_sink_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
                                _ptr(kv_lens), _ptr(block_table), block_table.shape[1], _ptr(sinks),
                                _ptr(out), _ptr(lse), B, total_q, int(max_q_len), Hq, Hkv, D,
                                page_size, num_pages, scale, int(bool(causal)), dt, _ptr(err_flag),
-                               _stream(stream))
+                               _ptr(workspace), ws_bytes, _stream(stream))
     _check("attn_sink_prefill", st)
     return out, lse
 

@@ -16,7 +16,9 @@ using namespace attn_sink;
 
 namespace {
 
-constexpr int kGb300Sms = 152;  // split heuristic assumes the GB300 SM count
+// SM count the decode split plan assumes when no device can be queried (a
+// host without a GPU asking for workspace sizes): a full GB300.
+constexpr int kDefaultSms = 152;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Limit of each pipeline wait inside the kernels, read when a call is enqueued.
@@ -27,6 +29,27 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// SM count of the current device (cached per device), or kDefaultSms when no
+// device can be queried.  The decode split plan and its workspace size use it,
+// so both must be asked with the same device current.
+int current_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();  // clear the error a missing device leaves behind
+    return kDefaultSms;
+  }
+  int sms = cache[dev].load(std::memory_order_relaxed);
+  if (sms > 0) return sms;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return kDefaultSms;
+  }
+  cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -137,7 +160,7 @@ DecodePlan plan_decode(int32_t B, int32_t Hkv, int32_t bt_stride, int32_t page_s
   // fp32 partials (and the merge) small.
   const long long groups = (Hkv + kHeadsPerCta - 1) / kHeadsPerCta;
   int cu = 128;
-  const long long target = 8LL * kGb300Sms;
+  const long long target = 8LL * current_sm_count();
   while (cu > 4 && static_cast<long long>(B) * groups * ((max_units + cu - 1) / cu) < target) cu /= 2;
   p.num_splits = 0;
   p.chunk_units = cu;
@@ -181,6 +204,12 @@ ATTN_SINK_API size_t attn_sink_decode_workspace_size(int32_t B, int32_t Hq, int3
   const DecodePlan p = plan_decode(B, Hkv, block_table_stride, page_size, num_splits);
   if (p.s_stride == 0) return 0;
   return partial_bytes(static_cast<long long>(B) * Hq, p.s_stride, nullptr);
+}
+
+ATTN_SINK_API size_t attn_sink_prefill_workspace_size(int32_t B, int32_t Hq, int32_t D,
+                                                      int32_t max_q_len) {
+  if (B <= 0 || Hq <= 0 || D != kHeadDim || max_q_len <= 0) return 0;
+  return kPrefillWorkspaceBytes;
 }
 
 }  // extern "C"
@@ -383,7 +412,8 @@ ATTN_SINK_API attn_sink_status attn_sink_prefill(
     const int32_t* kv_lens, const int32_t* block_table, int32_t block_table_stride,
     const float* sinks, void* out, float* lse, int32_t B, int32_t total_q, int32_t max_q_len,
     int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages, float scale,
-    int32_t causal, attn_sink_dtype dtype, int32_t* err_flag, void* stream) {
+    int32_t causal, attn_sink_dtype dtype, int32_t* err_flag, void* workspace,
+    size_t workspace_bytes, void* stream) {
   attn_sink_status st =
       check_shapes(B, Hq, Hkv, D, page_size, num_pages, block_table_stride, dtype);
   if (st != ATTN_SINK_OK) return st;
@@ -424,6 +454,9 @@ ATTN_SINK_API attn_sink_status attn_sink_prefill(
     return from_cuda(launch_simt_fp32(a, s));
   }
 
+  if (!workspace || workspace_bytes < kPrefillWorkspaceBytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_SINK_ERR_WORKSPACE;
   CUtensorMap q_map, k_map, v_map;
   const uint64_t rows = static_cast<uint64_t>(num_pages) * page_size;
   if (!make_map_q(&q_map, q, static_cast<uint64_t>(total_q), static_cast<uint64_t>(Hq),
@@ -451,6 +484,7 @@ ATTN_SINK_API attn_sink_status attn_sink_prefill(
   a.scale_log2 = scale * kLog2e;
   a.causal = causal;
   a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  a.tile_ctr = static_cast<unsigned long long*>(workspace);
   return from_cuda(launch_prefill_bf16(a, q_map, k_map, v_map, s));
 }
 

@@ -117,7 +117,11 @@ struct PrefillArgs {
   float scale_log2;
   int causal;
   uint64_t wait_limit_ns;      // limit of each pipeline wait (drains keep kWaitLimitNs)
+  unsigned long long* tile_ctr;  // work-tile claim counter (workspace), zeroed before launch
 };
+
+// Bytes of workspace the bf16 prefill uses (its work-tile claim counter).
+constexpr size_t kPrefillWorkspaceBytes = 256;
 
 cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
                                 const CUtensorMap& k_map, const CUtensorMap& v_map,

@@ -11,9 +11,11 @@
 // heads of KV group g (GQA packing), so each K/V tile is read once per 2*128/G
 // tokens of the whole group.  The grid has one CTA per SM.  Work tiles form a
 // list ordered longest rows first (the last query block of every sequence,
-// then the one before, ...), so the rows with the most keys start first; CTA c
-// takes one tile per round of gridDim.x tiles, position c in even rounds and
-// gridDim.x - 1 - c in odd ones, which evens out the CTAs' sums.
+// then the one before, ...).  CTAs claim tiles from that list at run time
+// through a counter in the caller's workspace, so a CTA that drew short tiles
+// takes more of them (greedy longest-first assignment); the Q/K producer warp
+// claims, and hands each claimed tile to the other roles through a small ring
+// in shared memory.
 //
 // Warp roles (384 threads):
 //   warps 0-3  softmax for Q tile 0, warps 4-7 softmax for Q tile 1: one
@@ -22,9 +24,9 @@
 //              registers, P (bf16) goes back into TMEM in its own columns and
 //              feeds P*V as the A operand.  The two warpgroups take turns in
 //              the exponential loop.
-//   warp 8     TMA producer of Q and K: per work tile the two Q tiles
-//              (double-buffered), then per 128-key tile eight 16-row page
-//              slices of K into a 4-stage ring.  It runs ahead across work
+//   warp 8     tile claims, then TMA producer of Q and K: per work tile the two
+//              Q tiles (double-buffered), then per 128-key tile eight 16-row
+//              page slices of K into a 4-stage ring.  It runs ahead across work
 //              tiles and reads the block-table entries one tile ahead.
 //   warps 9-10 one MMA-issuing warp per Q tile (warp 9 also owns TMEM).
 //   warp 11    TMA producer of V, in step with warp 8.  A 2 KB page slice
@@ -42,7 +44,6 @@
 // warpgroup hands S back (s_free) as soon as it has loaded it, so S(j+1) is
 // computed while the softmax of tile j runs.  Every barrier phase is counted
 // across work tiles, so the pipeline never drains between them.
-#include "exp2_poly.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -86,20 +87,21 @@ constexpr int kOffBar = kOffKV + kStages * kStageBytes;
 // Per-sequence lengths and per-head sinks are copied to shared memory when
 // they fit, so that decoding a work tile costs no global-memory round trip.
 constexpr int kMetaSeqs = 1024, kMetaHeads = 256;
-constexpr int kOffMeta = kOffBar + 256;
+constexpr int kBarBytes = 512;
+constexpr int kOffMeta = kOffBar + kBarBytes;
 constexpr int kMetaBytes = ((2 * kMetaSeqs + 1 + kMetaHeads) * 4 + 255) / 256 * 256;
-constexpr int kSmemBytes = kOffMeta + kMetaBytes + 1024;
+constexpr int kOffSort = kOffMeta + kMetaBytes;
+constexpr int kSortBytes = 2048 * 4 + 256;  // the sorted query blocks and their counter
+constexpr int kSmemBytes = kOffSort + kSortBytes + 1024;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// O is rescaled whenever a row's running maximum grows, so the largest p of a
-// row is exactly 1 and its bf16 rounding (for the P*V MMA) is exact.
-constexpr float kRescaleLog2 = 0.f;
-// Of every kPolyDen pairs of exponentials, kPolyNum go through the polynomial
-// on the FMA pipe and the rest through MUFU ex2.  On GB300 MUFU ex2 issues
-// every 4 clocks per SMSP and the split measured slower, so it is off.
-constexpr int kPolyNum = 0, kPolyDen = 4;
+// Claimed work tiles in flight between the claiming warp and the other roles.
+constexpr int kTileRing = 4;
+// Warps that read every claimed tile: the V producer, the MMA warps and the
+// softmax warps.
+constexpr int kTileReaders = 1 + kQTiles + kSoftmaxWarps;
 
 struct alignas(8) Bars {
   uint64_t q_full[kQBufs];
@@ -113,12 +115,15 @@ struct alignas(8) Bars {
   uint64_t o_free[kQTiles];   // the warpgroup has read the work tile's final O
   uint64_t exp_turn[kQTiles]; // warpgroup q may run its exponentials (token passed between them)
   uint64_t mma_done;
+  uint64_t tile_full[kTileRing];   // the slot holds the next claimed tile
+  uint64_t tile_empty[kTileRing];  // every reader has taken the slot's tile
+  long long tile_slot[kTileRing];  // claimed tile index, or -1: no tile left
   uint32_t unit_ok[kStages];  // bit u: 16-key unit u of the stage's tile was loaded
   uint32_t s_uok[kQTiles];    // unit_ok of the stage the current S was computed from
   uint32_t tmem_base;
   int abort_word;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= kBarBytes, "barrier block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // Where the per-sequence lengths and the sinks are read from.
@@ -131,18 +136,24 @@ struct Meta {
 // A work tile, derived identically by every role from its linear index.
 struct WorkTile {
   int b, g, q_start, q_len, tok0, kv_raw, kv_len, n_kv;
-  long long first_pos;  // absolute position of the tile's first query
+  int first_pos;  // absolute position of the tile's first query (fits: kv_len, q_len < 2^31)
 };
 
-// Work tile of round `round` for this CTA.  Rounds alternate direction (CTA c
-// takes position c of even rounds and gridDim.x - 1 - c of odd ones), so a CTA
-// that drew one of the longest tiles of a round draws one of the shortest of
-// the next.  Tiles grow with the round, so a tile past n_tiles ends the loop.
-__device__ __forceinline__ long long snake_tile(long long round) {
-  const long long pos = (round & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x;
-  return round * gridDim.x + pos;
+// Query block r of sequence b (r = 0 is the last block): its first query
+// token and the number of 128-key tiles its rows see.
+__device__ __forceinline__ int block_key_tiles(const PrefillArgs& a, int q_len, int kv_len, int n_blocks,
+                                               int r, int tok_per_cta, int& tok0) {
+  tok0 = (n_blocks - 1 - r) * tok_per_cta;
+  const long long last_pos =
+      static_cast<long long>(kv_len) - q_len + min(tok0 + tok_per_cta, q_len) - 1;
+  long long key_end = kv_len;
+  if (a.causal && key_end > last_pos + 1) key_end = last_pos + 1;
+  if (key_end < 0) key_end = 0;
+  return static_cast<int>((key_end + kKeys - 1) / kKeys);
 }
 
+// Work tile t of the row-major list: t = r * (B * Hkv) + b * Hkv + g.
+// Returns false when sequence b has no query block r.
 __device__ __forceinline__ bool decode_tile(const PrefillArgs& a, const Meta& m, long long t,
                                             int tok_per_cta, WorkTile& w) {
   const long long heads = static_cast<long long>(a.B) * a.Hkv;
@@ -154,16 +165,114 @@ __device__ __forceinline__ bool decode_tile(const PrefillArgs& a, const Meta& m,
   w.q_len = m.cu_seqlens_q[w.b + 1] - w.q_start;
   const int n_blocks = w.q_len > 0 ? (w.q_len + tok_per_cta - 1) / tok_per_cta : 0;
   if (r >= n_blocks) return false;
-  w.tok0 = (n_blocks - 1 - r) * tok_per_cta;
   w.kv_raw = max(0, m.kv_lens[w.b]);
   w.kv_len = min(w.kv_raw, a.bt_stride * a.page_size);  // keys beyond the table row are not read
-  w.first_pos = static_cast<long long>(w.kv_len) - w.q_len + w.tok0;
-  const long long last_pos =
-      static_cast<long long>(w.kv_len) - w.q_len + min(w.tok0 + tok_per_cta, w.q_len) - 1;
-  long long key_end = w.kv_len;
-  if (a.causal && key_end > last_pos + 1) key_end = last_pos + 1;
-  if (key_end < 0) key_end = 0;
-  w.n_kv = static_cast<int>((key_end + kKeys - 1) / kKeys);
+  w.n_kv = block_key_tiles(a, w.q_len, w.kv_len, n_blocks, r, tok_per_cta, w.tok0);
+  w.first_pos = w.kv_len - w.q_len + w.tok0;
+  return true;
+}
+
+// The claim order.  Query blocks (b, r) sorted by the key tiles their rows
+// see, most first, so that dynamic claims assign the longest work first
+// (greedy longest-processing-time).  A sort key packs (2047 - cost, r, b) into
+// 21 + 11 + 10 bits; sorting the keys ascending gives cost descending, then
+// the row-major order.  Costs above 2047 key tiles compare equal (their order
+// is then row-major), which leaves the list valid.
+constexpr int kSortMax = 2048;  // query blocks the sorted list holds
+__device__ __forceinline__ uint32_t block_sort_key(int cost, int r, int b) {
+  return (static_cast<uint32_t>(2047 - min(cost, 2047)) << 21) | (static_cast<uint32_t>(r) << 10) |
+         static_cast<uint32_t>(b);
+}
+
+// Builds the sorted list in shared memory (all threads of the CTA).  Every
+// CTA builds the same list: the keys are distinct, so their sorted order does
+// not depend on where each thread placed them.  Returns the number of query
+// blocks, or -1 when the list is not used: all sequences alike (the row-major
+// list is then already in cost order), more than kSortMax blocks, or the
+// metadata is not in shared memory.
+__device__ __forceinline__ int build_sorted_blocks(const PrefillArgs& a, const Meta& m, bool meta_in_smem,
+                                   int tok_per_cta, uint32_t* keys, int* counter) {
+  if (!meta_in_smem || a.B > 1024) return -1;
+  if (threadIdx.x == 0) *counter = 0;
+  // all sequences alike?
+  int differs = 0;
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x)
+    differs |= (m.cu_seqlens_q[b + 1] - m.cu_seqlens_q[b] != m.cu_seqlens_q[1] - m.cu_seqlens_q[0]) ||
+               (m.kv_lens[b] != m.kv_lens[0]);
+  if (__syncthreads_or(differs) == 0) return -1;
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+    const int q_len = m.cu_seqlens_q[b + 1] - m.cu_seqlens_q[b];
+    const int n_blocks = q_len > 0 ? (q_len + tok_per_cta - 1) / tok_per_cta : 0;
+    const int kv_len = min(max(0, m.kv_lens[b]), a.bt_stride * a.page_size);
+    for (int r = 0; r < n_blocks; ++r) {
+      const int slot = atomicAdd(counter, 1);
+      if (slot >= kSortMax) break;
+      int tok0;
+      keys[slot] = block_sort_key(block_key_tiles(a, q_len, kv_len, n_blocks, r, tok_per_cta, tok0), r, b);
+    }
+  }
+  __syncthreads();
+  const int n = *counter;
+  if (n > kSortMax) return -1;
+  int pow2 = 1;
+  while (pow2 < n) pow2 <<= 1;
+  for (int i = n + threadIdx.x; i < pow2; i += blockDim.x) keys[i] = 0xFFFFFFFFu;
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int k = 2; k <= pow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint32_t x = keys[i], y = keys[l];
+          if (((i & k) == 0) == (x > y)) {
+            keys[i] = y;
+            keys[l] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  return n;
+}
+
+// Claims the next work tile (warp-collective; every lane returns the same
+// row-major tile index, or -1 when every tile has been claimed).  With the
+// sorted list (n_sorted >= 0) claim k is query block keys[k / Hkv], KV head
+// k % Hkv; without it the claims walk the row-major list and pass over the
+// indices past a sequence's last block.
+__device__ __forceinline__ long long claim_tile(const PrefillArgs& a, const Meta& m, long long n_tiles,
+                                                int tok_per_cta, const uint32_t* keys, int n_sorted) {
+  const int lane = threadIdx.x & 31;
+  const long long n_claims = n_sorted >= 0 ? static_cast<long long>(n_sorted) * a.Hkv : n_tiles;
+  for (;;) {
+    unsigned long long c = 0;
+    if (lane == 0) c = atomicAdd(a.tile_ctr, 1ull);
+    const long long k = static_cast<long long>(__shfl_sync(0xffffffffu, c, 0));
+    if (k >= n_claims) return -1;
+    if (n_sorted >= 0) {
+      const uint32_t key = keys[k / a.Hkv];
+      const int r = static_cast<int>((key >> 10) & 0x7FFu), b = static_cast<int>(key & 0x3FFu);
+      return static_cast<long long>(r) * a.B * a.Hkv + static_cast<long long>(b) * a.Hkv + k % a.Hkv;
+    }
+    WorkTile w;
+    if (decode_tile(a, m, k, tok_per_cta, w)) return k;
+  }
+}
+
+// A reader role takes claimed tile number i from the ring (warp-collective).
+// Returns false when the pipeline aborted; t = -1 means no tile is left.
+template <bool kPoll>
+__device__ __forceinline__ bool take_tile(Bars* bars, int i, long long& t, volatile int* abort_word,
+                                          const PrefillArgs& a) {
+  const int slot = i % kTileRing;
+  const bool ready = mbar_wait<kPoll>(&bars->tile_full[slot], (i / kTileRing) & 1, abort_word,
+                                      a.err_flag, a.wait_limit_ns);
+  if (!__all_sync(0xffffffffu, ready)) return false;
+  t = *reinterpret_cast<volatile long long*>(&bars->tile_slot[slot]);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&bars->tile_empty[slot]);
   return true;
 }
 
@@ -202,6 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->exp_turn[q], 4);  // one arrive per warp of the other warpgroup
     }
     mbar_init(&bars->mma_done, kQTiles);
+    for (int i = 0; i < kTileRing; ++i) {
+      mbar_init(&bars->tile_full[i], 1);               // the claiming warp
+      mbar_init(&bars->tile_empty[i], kTileReaders);   // one arrive per reader warp
+    }
     bars->abort_word = 0;
     fence_barrier_init();
   }
@@ -219,6 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < a.Hq; i += kThreads) sinks_s[i] = a.sinks[i];
     meta = Meta{cu_s, kvl_s, sinks_s};
   }
+  uint32_t* sort_keys = reinterpret_cast<uint32_t*>(base + kOffSort);
+  __syncthreads();  // the metadata is in place
+  const int n_sorted = build_sorted_blocks(a, meta, a.B <= kMetaSeqs && a.Hq <= kMetaHeads,
+                                           tok_per_cta, sort_keys,
+                                           reinterpret_cast<int*>(base + kOffSort + 2048 * 4));
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -241,9 +359,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t reuse = l2_policy_evict_last();   // K/V tiles serve every later query block
     int qw = 0, kv_it = 0;
     bool ok = true;
-    for (long long rnd = 0, t = snake_tile(0); ok && t < n_tiles; t = snake_tile(++rnd)) {
+    for (int i = 0; ok; ++i) {
+      long long t;
+      if (is_k) {
+        // Claim the next tile and publish it to the other roles.
+        t = claim_tile(a, meta, n_tiles, tok_per_cta, sort_keys, n_sorted);
+        const int slot = i % kTileRing;
+        if (i >= kTileRing) {
+          const bool ready = mbar_wait<kPoll>(&bars->tile_empty[slot], ((i / kTileRing) + 1) & 1,
+                                              abort_word, a.err_flag, a.wait_limit_ns);
+          ok = __all_sync(0xffffffffu, ready);
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          bars->tile_slot[slot] = t;
+          mbar_arrive(&bars->tile_full[slot]);  // release: the slot is written
+        }
+        __syncwarp();
+      } else {
+        ok = take_tile<kPoll>(bars, i, t, abort_word, a);
+        if (!ok) break;
+      }
+      if (t < 0) break;
       WorkTile w;
-      if (!decode_tile(a, meta, t, tok_per_cta, w)) continue;
+      decode_tile(a, meta, t, tok_per_cta, w);  // a claimed tile always holds query rows
       if (is_k && w.kv_len < w.kv_raw && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
       if (w.n_kv == 0) continue;
       if (is_k) {
@@ -353,9 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int qw = 0, kv_it = 0, it = 0, ow = 0;
     bool ok = true;
-    for (long long rnd = 0, t = snake_tile(0); ok && t < n_tiles; t = snake_tile(++rnd)) {
+    for (int i = 0; ok; ++i) {
+      long long t;
+      ok = take_tile<kPoll>(bars, i, t, abort_word, a);
+      if (!ok || t < 0) break;
       WorkTile w;
-      if (!decode_tile(a, meta, t, tok_per_cta, w) || w.n_kv == 0) continue;
+      decode_tile(a, meta, t, tok_per_cta, w);
+      if (w.n_kv == 0) continue;
       const int qb = qw % kQBufs;
       // Q loaded, the first K/V tile in, and the previous S read out of TMEM.
       ok = wait_all(&bars->q_full[qb], (qw / kQBufs) & 1) &&
@@ -410,20 +553,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one computes exponentials while the other loads S, reduces and stores P.
     // Warpgroup 1 hands warpgroup 0 the first turn.
     if (kQTiles > 1 && q == 1 && lane == 0) mbar_arrive(&bars->exp_turn[0]);
-    int kv_it = 0, it = 0;
+    // Key tiles consumed so far: every S, P*V and stage this warpgroup has
+    // gone through (all three advance together).
+    int it = 0;
     bool ok = true;
-    for (long long rnd = 0, t = snake_tile(0); ok && t < n_tiles; t = snake_tile(++rnd)) {
+    for (int i = 0; ok; ++i) {
+      long long t;
+      ok = take_tile<kPoll>(bars, i, t, abort_word, a);
+      if (!ok || t < 0) break;
       WorkTile w;
-      if (!decode_tile(a, meta, t, tok_per_cta, w)) continue;
+      decode_tile(a, meta, t, tok_per_cta, w);
       const int tok = w.tok0 + q * tok_per_tile + r / a.group;
       const int head = w.g * a.group + r % a.group;
       const bool row_valid = tok < w.q_len;
-      const long long pos = static_cast<long long>(w.kv_len) - w.q_len + tok;
+      const int pos = w.kv_len - w.q_len + tok;  // fits: kv_len, q_len < 2^31
       float m_run = meta.sinks[head] * kLog2e;  // the sink is the initial running max ...
       float d_run = 1.f;                     // ... with running sum e^0 = 1
       for (int j = 0; j < w.n_kv; ++j) {
-        const int cur = kv_it + j, u = it + j;
-        const int st = cur % kStages;
+        const int u = it + j;
+        const int st = u % kStages;
         // s_full completes after the MMA warp saw the stage's kv_full: the
         // stage has landed, and s_uok holds its unit mask.
         const bool ready = mbar_wait<kPoll>(&bars->s_full[q], u & 1, abort_word, a.err_flag, a.wait_limit_ns);
@@ -474,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // after the row's position.  Skipped pages (rare) are cleared unit
           // by unit.
           int lim = w.kv_len - key_base;
-          if (a.causal) lim = min(lim, static_cast<int>(pos - key_base + 1));
+          if (a.causal) lim = min(lim, pos - key_base + 1);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -500,7 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx = max3f(max3f(ch[0], ch[1], ch[2]), max3f(ch[3], ch[4], ch[5]), fmaxf(ch[6], ch[7]));
         }
         const float m_new = fmaxf(m_run, mx * scale_log2);
-        const bool resc = m_new > m_run + kRescaleLog2;
+        // O is rescaled whenever a row's running maximum grows, so the largest p of
+        // a row is exactly 1 and its bf16 rounding (for the P*V MMA) is exact.
+        const bool resc = m_new > m_run;
         float alpha = 1.f;
         if (resc) {
           alpha = fast_exp2(m_run - m_new);
@@ -527,13 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        scale2, negm2);
             float x0, x1;
             f2_unpack(x2, x0, x1);
-            float e0, e1;
-            if (((c * 16 + i / 2) % kPolyDen) < kPolyNum) {
-              exp2_poly_pair(x0, x1, e0, e1);
-            } else {
-              e0 = fast_exp2(x0);
-              e1 = fast_exp2(x1);
-            }
+            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
             const uint32_t pk = pack_bf16x2(e0, e1);
             p[c >> 1][(c & 1) * 16 + i / 2] = pk;
             ex2[(i >> 1) & 3] = f2_add(ex2[(i >> 1) & 3], f2_pack(e0, e1));
@@ -641,7 +785,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.lse)
           a.lse[grow] = (d_run > 0.f && m_run != -INFINITY) ? (m_run + __log2f(d_run)) * kLn2 : -INFINITY;
       }
-      kv_it += w.n_kv;
       it += w.n_kv;
     }
   }
@@ -677,6 +820,10 @@ cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
   const unsigned grid = static_cast<unsigned>(n_tiles < sms ? n_tiles : sms);
+  // The claim counter starts at zero on every launch (a memset node when the
+  // stream is being captured).
+  e = cudaMemsetAsync(a.tile_ctr, 0, sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, a, n_tiles);
   return cudaGetLastError();
 }

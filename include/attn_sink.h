@@ -98,6 +98,16 @@ typedef enum {
  *  max_q_len    host upper bound of any sequence's q_len (sizes the grid).
  *  scale        softmax scale applied to q.k (typically 1/sqrt(D)).
  *  causal       1 = causal (bottom-right aligned), 0 = every key visible.
+ *  workspace    device scratch of at least attn_sink_prefill_workspace_size()
+ *               bytes, 256-byte aligned (bf16: required, ATTN_SINK_ERR_WORKSPACE
+ *               otherwise; fp32: unused, may be NULL).  It holds the counter
+ *               from which the kernel's CTAs claim work tiles at run time
+ *               ("Embedding Cepat di GPU", section "Manajemen Grafik CUDA":
+ *               per-batch scheduling state lives on the device, so the launch
+ *               depends only on host integers).  The call zeroes it on the
+ *               stream before the kernel (a memset node under stream capture);
+ *               no contents need to be preserved.  Calls that overlap on the
+ *               GPU need separate workspaces.
  */
 ATTN_SINK_API attn_sink_status attn_sink_prefill(const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* cu_seqlens_q, const int32_t* kv_lens,
@@ -106,7 +116,12 @@ ATTN_SINK_API attn_sink_status attn_sink_prefill(const void* q, const void* k_ca
                                    int32_t total_q, int32_t max_q_len, int32_t Hq, int32_t Hkv,
                                    int32_t D, int32_t page_size, int32_t num_pages, float scale,
                                    int32_t causal, attn_sink_dtype dtype, int32_t* err_flag,
-                                   void* stream);
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_sink_prefill needs for these arguments (0 when the
+ * call has nothing to do).  Pure host function. */
+ATTN_SINK_API size_t attn_sink_prefill_workspace_size(int32_t B, int32_t Hq, int32_t D,
+                                                      int32_t max_q_len);
 
 /*
  * Paged-KV decode, one query token per sequence, optionally split along the
@@ -164,7 +179,11 @@ ATTN_SINK_API attn_sink_status attn_sink_decode_append(const void* q, const void
                                          size_t workspace_bytes, void* stream);
 
 /* Workspace bytes attn_sink_decode needs for these arguments (0 when it needs
- * none).  Pure host function. */
+ * none).  Host function; it reads no device memory.  With num_splits = 0 the
+ * chunk length, and so the number of partial states per row, depends on Hkv,
+ * the table row length (block_table_stride * page_size keys) and the current
+ * device's SM count, so ask with the device current that the call will run
+ * on (with no device, a 152-SM GB300 is assumed). */
 ATTN_SINK_API size_t attn_sink_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
                                        int32_t block_table_stride, int32_t page_size,
                                        int32_t num_splits);

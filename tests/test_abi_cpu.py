@@ -25,7 +25,8 @@ def lib():
 def test_header_declares_entry_points():
     names = _declared()
     for n in ("attn_sink_prefill", "attn_sink_decode", "attn_sink_merge",
-              "attn_sink_decode_workspace_size", "attn_sink_status_string"):
+              "attn_sink_decode_workspace_size", "attn_sink_prefill_workspace_size",
+              "attn_sink_status_string"):
         assert n in names
 
 
@@ -103,3 +104,42 @@ def test_host_validation_rejects_before_launch(lib):
     assert _call_decode(lib, S=4, ws=None, wsb=0) == 3         # missing workspace
     assert _call_decode(lib, S=4, ws=256 + 16, wsb=1 << 20) == 3   # misaligned workspace
     assert _call_decode(lib, B=0) == 0                         # empty batch is a no-op
+
+
+def test_prefill_workspace_size_is_host_only(lib):
+    f = lib.attn_sink_prefill_workspace_size
+    f.argtypes = [ctypes.c_int32] * 4
+    f.restype = ctypes.c_size_t
+    assert f(8, 64, 64, 4096) == 256          # the work-tile claim counter
+    assert f(0, 64, 64, 4096) == 0            # nothing to do
+    assert f(8, 64, 64, 0) == 0
+    assert f(8, 64, 128, 4096) == 0           # unsupported head dim
+
+
+def _call_prefill(lib, **kw):
+    # Fake, 256-aligned addresses: every call below is rejected by the host
+    # checks before anything touches them.
+    args = dict(q=256, k=512, v=768, cu=1024, kv=1280, bt=1536, stride=4, sinks=1792, out=2048,
+                lse=None, B=2, total_q=8, max_q=4, Hq=8, Hkv=2, D=64, ps=16, pages=8, scale=0.125,
+                causal=1, dt=0, err=None, ws=4096, wsb=256, stream=None)
+    args.update(kw)
+    f = lib.attn_sink_prefill
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    f.argtypes = [vp] * 6 + [i32, vp, vp, vp] + [i32] * 8 + [ctypes.c_float, i32, i32, vp, vp,
+                                                              ctypes.c_size_t, vp]
+    f.restype = i32
+    a = args
+    return f(a["q"], a["k"], a["v"], a["cu"], a["kv"], a["bt"], a["stride"], a["sinks"], a["out"],
+             a["lse"], a["B"], a["total_q"], a["max_q"], a["Hq"], a["Hkv"], a["D"], a["ps"],
+             a["pages"], a["scale"], a["causal"], a["dt"], a["err"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_prefill_host_validation_rejects_before_launch(lib):
+    assert _call_prefill(lib, q=None) == 1                     # null pointer
+    assert _call_prefill(lib, causal=2) == 1
+    assert _call_prefill(lib, D=128) == 2                      # unsupported head dim
+    assert _call_prefill(lib, ws=None, wsb=0) == 3             # bf16 needs the workspace
+    assert _call_prefill(lib, wsb=128) == 3                    # too small
+    assert _call_prefill(lib, ws=4096 + 64) == 3               # misaligned
+    assert _call_prefill(lib, B=0) == 0                        # empty batch is a no-op
+    assert _call_prefill(lib, max_q=0, ws=None, wsb=0) == 0    # no rows: nothing to do

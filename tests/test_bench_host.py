@@ -49,3 +49,45 @@ def test_reference_arm_two_ranks_gloo():
     res = json.loads(lines[0])
     assert res["impl"] == "reference" and res["n_gpus"] == 2 and res["value"] > 0
     assert res["cpu_baseline"]["kind"] == "oracle"
+
+
+def _timing_rank(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import time
+
+        def clock():
+            return time.perf_counter, lambda t0: (time.perf_counter() - t0) * 1e3
+        delay = 0.02 * (rank + 1)                   # rank 1 is the slow one
+        calls = []
+
+        def step():
+            calls.append(1)
+            time.sleep(delay)
+        ms = bench.time_region(step, 3, 2, sync=lambda: None, barrier=dist.barrier,
+                               reduce_max=bench.make_reduce_max(world, "cpu"), clock=clock)
+        q.put((rank, ms, len(calls)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_timed_region_max_over_two_gloo_ranks():
+    """The timed region of the GPU arm (barrier on both sides, max over ranks) run
+    by two CPU ranks over gloo: both ranks report the slower rank's time, and
+    exactly warmup + steps calls happen per rank."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_timing_rank, args=(r, 2, 29541, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, ms0, n0), (r1, ms1, n1) = res
+    assert n0 == n1 == 5
+    assert ms0 == ms1                                  # the same maximum on both ranks
+    assert 3 * 40 <= ms0 < 3 * 40 + 200                # rank 1's three 40 ms steps

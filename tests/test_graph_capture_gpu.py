@@ -76,10 +76,14 @@ def test_prefill_graph_replay_matches_eager(cuda_lib):
     db = DeviceBatch(batch)
     out = torch.empty_like(db.q)
     lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device="cuda")
+    # One workspace for the eager calls and the replays: the call's memset node
+    # restarts the tile-claim counter on every replay.
+    wsb = torch.empty(gas.prefill_workspace_size(batch.B, batch.Hq, batch.D, int(q_lens.max())),
+                      dtype=torch.uint8, device="cuda")
 
     def call():
         gas.prefill(db.q, db.k, db.v, db.cu, db.kv_lens, db.bt, db.sinks, max_q_len=int(q_lens.max()),
-                    scale=batch.scale, out=out, lse=lse, err_flag=db.err)
+                    scale=batch.scale, out=out, lse=lse, workspace=wsb, err_flag=db.err)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
