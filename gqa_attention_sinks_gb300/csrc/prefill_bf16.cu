@@ -758,6 +758,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = d_run > 0.f ? 1.f / d_run : 0.f;
         const long long grow = static_cast<long long>(w.q_start + tok) * a.Hq + head;
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim;
+        // The output is written once and read by no later tile: evict-first,
+        // so it does not push the K/V tiles that later query blocks re-read
+        // out of L2.
+        const uint64_t out_policy = l2_policy_evict_first();
         if ((reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) {
           // 32-byte stores: whole sectors, four instructions per row.
 #pragma unroll
@@ -767,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               pk[e] = pack_bf16x2(__uint_as_float(o[h][i + 2 * e]) * inv, __uint_as_float(o[h][i + 2 * e + 1]) * inv);
-            st_global_v8(orow + v * 16, pk);
+            st_global_v8_hint(orow + v * 16, pk, out_policy);
           }
         } else {
           uint4* dst = reinterpret_cast<uint4*>(orow);
@@ -779,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             o4.y = pack_bf16x2(__uint_as_float(o[h][i + 2]) * inv, __uint_as_float(o[h][i + 3]) * inv);
             o4.z = pack_bf16x2(__uint_as_float(o[h][i + 4]) * inv, __uint_as_float(o[h][i + 5]) * inv);
             o4.w = pack_bf16x2(__uint_as_float(o[h][i + 6]) * inv, __uint_as_float(o[h][i + 7]) * inv);
-            dst[v] = o4;
+            st_global_v4_hint(dst + v, o4, out_policy);
           }
         }
         if (a.lse)

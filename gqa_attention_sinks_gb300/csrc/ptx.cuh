@@ -218,6 +218,20 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
                : "memory");
 }
 
+// The same store with an L2 eviction-priority policy (createpolicy): output
+// that no later read of this kernel needs should not displace reused data.
+__device__ __forceinline__ void st_global_v8_hint(void* p, const uint32_t (&v)[8], uint64_t policy) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8}, %9;" ::"l"(p),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+               "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v4_hint(void* p, const uint4& v, uint64_t policy) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.b32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
+
 // True in exactly one active lane of the warp (warp-collective).
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;
