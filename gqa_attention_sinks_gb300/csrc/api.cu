@@ -216,13 +216,18 @@ ATTN_SINK_API size_t attn_sink_prefill_workspace_size(int32_t B, int32_t Hq, int
 
 namespace {
 
-// Decode, optionally appending the step's key and value first (k_new != null).
-attn_sink_status decode_impl(
-    const void* q, const void* k_new, const void* v_new, const void* k_cache, const void* v_cache,
-    const int32_t* kv_lens, const int32_t* block_table, int32_t block_table_stride,
-    const float* sinks, void* out, float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
-    int32_t page_size, int32_t num_pages, float scale, int32_t num_splits, attn_sink_dtype dtype,
-    int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream) {
+}  // namespace
+
+namespace attn_sink {
+
+// Host-side checks of a decode call that need no workspace (shared with the
+// static-scratch entry point, so both report the same status for a bad call).
+attn_sink_status decode_validate(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* kv_lens, const int32_t* block_table,
+                                 int32_t block_table_stride, const float* sinks, const void* out,
+                                 int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                                 int32_t num_pages, float scale, int32_t num_splits,
+                                 attn_sink_dtype dtype) {
   attn_sink_status st =
       check_shapes(B, Hq, Hkv, D, page_size, num_pages, block_table_stride, dtype);
   if (st != ATTN_SINK_OK) return st;
@@ -231,6 +236,24 @@ attn_sink_status decode_impl(
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return ATTN_SINK_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > 256 || !std::isfinite(scale)) return ATTN_SINK_ERR_INVALID_ARG;
+  return ATTN_SINK_OK;
+}
+
+}  // namespace attn_sink
+
+namespace {
+
+// Decode, optionally appending the step's key and value first (k_new != null).
+attn_sink_status decode_impl(
+    const void* q, const void* k_new, const void* v_new, const void* k_cache, const void* v_cache,
+    const int32_t* kv_lens, const int32_t* block_table, int32_t block_table_stride,
+    const float* sinks, void* out, float* lse, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+    int32_t page_size, int32_t num_pages, float scale, int32_t num_splits, attn_sink_dtype dtype,
+    int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream) {
+  const attn_sink_status st =
+      decode_validate(q, k_cache, v_cache, kv_lens, block_table, block_table_stride, sinks, out, B,
+                      Hq, Hkv, D, page_size, num_pages, scale, num_splits, dtype);
+  if (st != ATTN_SINK_OK) return st;
   if (B == 0) return ATTN_SINK_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int group = Hq / Hkv;

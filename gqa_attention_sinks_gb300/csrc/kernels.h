@@ -6,7 +6,18 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "attn_sink.h"
+
 namespace attn_sink {
+
+// Host-side argument checks of attn_sink_decode (everything but the
+// workspace), shared by the decode entry points.
+attn_sink_status decode_validate(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* kv_lens, const int32_t* block_table,
+                                 int32_t block_table_stride, const float* sinks, const void* out,
+                                 int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                                 int32_t num_pages, float scale, int32_t num_splits,
+                                 attn_sink_dtype dtype);
 
 constexpr int kHeadDim = 64;     // the only head dimension the kernels are built for
 constexpr int kUnitTokens = 16;  // keys per TMA box: one 16-row slice of a page

@@ -219,9 +219,13 @@ ATTN_SINK_API attn_sink_status attn_sink_merge(const float* o_parts, const float
  *  - A call whose partials need more than ATTN_SINK_STATIC_SCRATCH_BYTES
  *    (attn_sink_decode_workspace_size reports the need) returns
  *    ATTN_SINK_ERR_WORKSPACE before enqueueing anything.
+ *  - Arguments are checked first, exactly as attn_sink_decode checks them, so
+ *    a bad call gets the same status from both entry points.
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress with that device current); make that first call
- *    before any stream capture on the device.
+ *    (cudaGetSymbolAddress with that device current), and looks it up again
+ *    when the device's context has changed (after cudaDeviceReset); make that
+ *    first call, and the first after a reset, before any stream capture on
+ *    the device.
  *  - All calls on a device share the array, which keeps the previous call's
  *    contents.  Nothing in it needs clearing: every partial the merge reads is
  *    written earlier in the same call.  Calls that overlap on the GPU (other

@@ -143,3 +143,29 @@ def test_prefill_host_validation_rejects_before_launch(lib):
     assert _call_prefill(lib, ws=4096 + 64) == 3               # misaligned
     assert _call_prefill(lib, B=0) == 0                        # empty batch is a no-op
     assert _call_prefill(lib, max_q=0, ws=None, wsb=0) == 0    # no rows: nothing to do
+
+
+def test_static_scratch_checks_arguments_like_decode(lib):
+    """Bad calls get the same status from the static-scratch entry point as from
+    attn_sink_decode: argument errors come before the scratch-size check."""
+    f = lib.attn_sink_decode_static_scratch
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    f.argtypes = [vp] * 5 + [i32, vp, vp, vp] + [i32] * 6 + [ctypes.c_float, i32, i32, vp, vp]
+    f.restype = i32
+
+    def call(**kw):
+        a = dict(q=256, k=512, v=768, kv=1024, bt=1280, stride=4096, sinks=1536, out=1792,
+                 lse=None, B=512, Hq=64, Hkv=8, D=64, ps=16, pages=8, scale=0.125, S=0, dt=0,
+                 err=None, stream=None)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["kv"], a["bt"], a["stride"], a["sinks"], a["out"],
+                 a["lse"], a["B"], a["Hq"], a["Hkv"], a["D"], a["ps"], a["pages"], a["scale"],
+                 a["S"], a["dt"], a["err"], a["stream"])
+
+    same = dict(B=512, Hq=64, Hkv=8, stride=4096)
+    for kw in (dict(S=300), dict(Hq=60), dict(q=None), dict(D=128), dict(scale=float("inf"))):
+        args = dict(same, **kw)
+        assert call(**args) == _call_decode(lib, **args), kw
+    assert call(S=300) == 1 and call(D=128) == 2
+    assert call() == 3                    # valid, but its partials exceed the static array
+    assert call(B=0) == 0
