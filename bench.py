@@ -10,7 +10,8 @@ sub-objects, each with its own roofline and CPU-oracle baseline:
   "long"     4 x 131072-key decode split into 32 chunks (GB/s)
   "mixed"    48 decode seqs (KV 1k..32k) + 4 x 512-token chunked prefills over
              prefixes up to 16k, 1% outlier keys: the decode part (GB/s) and the
-             chunked-prefill part (TFLOP/s), each against its own roofline
+             chunked-prefill part (TFLOP/s), each against its own roofline, and
+             the whole batch as one attn_sink_mixed launch ("one_launch")
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload all|decode|prefill|long|mixed] [--no-cpu-baseline]
@@ -405,6 +406,42 @@ class GpuArm:
                 "gpu_launches": steps, "clocks": clocks}
         return part, step
 
+    def mixed_one_launch(self, batch, num_decode, steps, dec_bytes, pre_flops):
+        """The whole mixed batch through attn_sink_mixed: decode rows and prefill
+        segments in one persistent launch (plus the merge of split decode rows)."""
+        torch, gas = self.torch, self.gas
+        d = dict(q=self.to_dev(batch.q), k=self.to_dev(batch.k_cache), v=self.to_dev(batch.v_cache),
+                 cu=self.to_dev(batch.cu_seqlens_q), kvl=self.to_dev(batch.kv_lens),
+                 bt=self.to_dev(batch.block_table), sinks=self.to_dev(batch.sinks))
+        out = torch.empty_like(d["q"])
+        lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=self.dev)
+        need = gas.mixed_workspace_size(num_decode, batch.Hq, batch.Hkv, batch.D,
+                                        batch.block_table.shape[1], batch.page_size)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.dev)
+        max_q = int(batch.q_lens[num_decode:].max())
+
+        def step():
+            gas.mixed(d["q"], d["k"], d["v"], d["cu"], d["kvl"], d["bt"], d["sinks"],
+                      num_decode=num_decode, max_q_len=max_q, scale=batch.scale, out=out, lse=lse,
+                      workspace=ws)
+
+        def run():
+            self.warm_clock(step)
+            total = self.timed(step, steps, self.args.warmup)
+            return total, self.per_call(step, steps)
+        (total_ms, call_ms), clocks = self.with_clocks(run)
+        # lower bound with perfect overlap: the decode bytes at the HBM peak and
+        # the prefill FLOPs at the bf16 peak run side by side
+        bound_ms = max(dec_bytes / (self.pk["hbm_gbs"] * 1e9), pre_flops / (self.pk["bf16_tflops"] * 1e12)) * 1e3
+        sum_ms = (dec_bytes / (self.pk["hbm_gbs"] * 1e9) + pre_flops / (self.pk["bf16_tflops"] * 1e12)) * 1e3
+        self.release(d)
+        return {"workload": "the whole mixed batch through attn_sink_mixed (one persistent launch "
+                            "+ merge)", "ms_per_step": round(total_ms / steps, 5), "steps": steps,
+                "call_ms": round(call_ms, 5), "overlap_bound_ms": round(bound_ms, 5),
+                "serial_bound_ms": round(sum_ms, 5),
+                "frac_of_overlap_bound": round(bound_ms / call_ms, 4), "gpu_launches": 2 * steps,
+                "clocks": clocks}
+
     def e2e_decode(self, batch, splits, d):
         """End to end through the C ABI: every step copies all its inputs from pinned
         host memory and reads its result back.  Two device input sets alternate, so
@@ -530,13 +567,17 @@ def run_ours(args, ws, rank, local):
             dstep()
             pstep()
         total = arm.timed(both, k, args.warmup)
+        one = arm.mixed_one_launch(m["single"], m["single"].meta["n_decode"], k,
+                                   dpart["bytes_per_step"], ppart["flops_per_step"])
         if want_cpu:
             dpart["cpu_baseline"] = cpu_oracle_rate(m["decode"], args.cpu_seconds / 2, "GB/s")
             ppart["cpu_baseline"] = cpu_oracle_rate(m["prefill"], args.cpu_seconds / 2, "TFLOP/s")
         arm.release(d)
         sub["mixed"] = {"workload": "mixed batch: decode part then chunked-prefill part, two "
                                     "launches on one stream",
-                        "ms_per_step": round(total / k, 5), "decode": dpart, "prefill": ppart}
+                        "ms_per_step": round(total / k, 5), "decode": dpart, "prefill": ppart,
+                        "one_launch": one}
+        one["vs_two_launches"] = round((total / k) / one["ms_per_step"], 3)
         del m
 
     if head is None:

@@ -17,8 +17,8 @@ import os
 
 import torch
 
-__all__ = ["load", "prefill", "decode", "decode_append", "merge", "decode_workspace_size",
-           "prefill_workspace_size", "status_string",
+__all__ = ["load", "prefill", "mixed", "decode", "decode_append", "merge", "decode_workspace_size",
+           "prefill_workspace_size", "mixed_workspace_size", "status_string",
            "set_wait_limit_ns", "AttnSinkError", "LIB_PATH", "FLAG_BAD_PAGE", "FLAG_TIMEOUT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +33,9 @@ _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c
 SIGNATURES = {
     "attn_sink_prefill": ([_vp] * 10 + [_i32] * 8 + [_f32, _i32, _i32, _vp, _vp, _sz, _vp], _i32),
     "attn_sink_prefill_workspace_size": ([_i32] * 4, _sz),
+    "attn_sink_mixed": ([_vp] * 6 + [_i32, _vp, _vp, _vp] + [_i32] * 9 + [_f32, _i32, _i32, _vp,
+                                                                         _vp, _sz, _vp], _i32),
+    "attn_sink_mixed_workspace_size": ([_i32] * 6, _sz),
     "attn_sink_decode": ([_vp] * 5 + [_i32, _vp, _vp, _vp] + [_i32] * 6 + [_f32, _i32, _i32, _vp,
                                                                          _vp, _sz, _vp], _i32),
     "attn_sink_decode_append": ([_vp] * 7 + [_i32, _vp, _vp, _vp] + [_i32] * 6 +
@@ -234,6 +237,49 @@ def prefill(q, k_cache, v_cache, cu_seqlens_q, kv_lens, block_table, sinks, *, m
                                page_size, num_pages, scale, int(bool(causal)), dt, _ptr(err_flag),
                                _ptr(workspace), ws_bytes, _stream(stream))
     _check("attn_sink_prefill", st)
+    return out, lse
+
+
+def mixed_workspace_size(num_decode, Hq, Hkv, D, block_table_stride, page_size):
+    """Bytes of scratch ``mixed`` needs for these arguments."""
+    return int(load().attn_sink_mixed_workspace_size(num_decode, Hq, Hkv, D, block_table_stride,
+                                                     page_size))
+
+
+def mixed(q, k_cache, v_cache, cu_seqlens_q, kv_lens, block_table, sinks, *, num_decode,
+          max_q_len, scale=None, causal=True, out=None, lse=None, workspace=None, err_flag=None,
+          stream=None):
+    """One launch for a ragged batch whose first num_decode sequences are
+    single-query decode rows and whose others are prefill segments (q_len up
+    to max_q_len).  q [total_q, Hq, D].  Returns (out, lse) like ``prefill``."""
+    lib = load()
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, name, q.dtype)
+    _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+    _dev(kv_lens, "kv_lens", torch.int32)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(sinks, "sinks", torch.float32)
+    total_q, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    B = kv_lens.shape[0]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    _dev(out, "out", q.dtype)
+    _dev(lse, "lse", torch.float32)
+    need = mixed_workspace_size(int(num_decode), Hq, Hkv, D, block_table.shape[1], page_size)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.attn_sink_mixed(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q),
+                             _ptr(kv_lens), _ptr(block_table), block_table.shape[1], _ptr(sinks),
+                             _ptr(out), _ptr(lse), B, int(num_decode), total_q, int(max_q_len), Hq,
+                             Hkv, D, page_size, num_pages, scale, int(bool(causal)), dt,
+                             _ptr(err_flag), _ptr(workspace), ws_bytes, _stream(stream))
+    _check("attn_sink_mixed", st)
     return out, lse
 
 

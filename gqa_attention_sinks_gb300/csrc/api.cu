@@ -95,17 +95,17 @@ bool make_map_q(CUtensorMap* map, const void* base, uint64_t total_q, uint64_t H
 }
 
 // 4-D bf16 tensor map over a paged NHD cache [num_pages, page_size, Hkv, 64]
-// ordered (dim, token in page, head, page), box {64, 16, kHeadsPerCta, 1}: one
-// copy brings a 16-token slice of kHeadsPerCta heads, each head's 16 rows
+// ordered (dim, token in page, head, page), box {64, 16, box_heads, 1}: one
+// copy brings a 16-token slice of box_heads heads, each head's 16 rows
 // contiguous (2 KB) in shared memory.  The head stride (128 B) is below the
 // token stride; TMA takes each dimension's stride as given.
 bool make_map_paged_heads(CUtensorMap* map, const void* base, uint64_t num_pages,
-                          uint64_t page_size, uint64_t Hkv) {
+                          uint64_t page_size, uint64_t Hkv, uint32_t box_heads = kHeadsPerCta) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {64, page_size, Hkv, num_pages};
   cuuint64_t strides[3] = {Hkv * 64 * 2, 64 * 2, page_size * Hkv * 64 * 2};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kUnitTokens), static_cast<cuuint32_t>(kHeadsPerCta), 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kUnitTokens), box_heads, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -169,6 +169,13 @@ DecodePlan plan_decode(int32_t B, int32_t Hkv, int32_t bt_stride, int32_t page_s
   return p;
 }
 
+// Partial slots per decode row of a mixed batch: the decode items of the
+// longest sequence the table row can hold.
+int mixed_slots(int32_t bt_stride, int32_t page_size) {
+  const long long units = (static_cast<long long>(bt_stride) * page_size + kUnitTokens - 1) / kUnitTokens;
+  return static_cast<int>(std::max(1LL, (units + kMixedChunkUnits - 1) / kMixedChunkUnits));
+}
+
 size_t partial_bytes(long long rows, int s_stride, size_t* o_bytes) {
   const size_t ob = align_up(static_cast<size_t>(rows) * s_stride * kHeadDim * sizeof(float), 256);
   const size_t lb = align_up(static_cast<size_t>(rows) * s_stride * sizeof(float), 256);
@@ -204,6 +211,17 @@ ATTN_SINK_API size_t attn_sink_decode_workspace_size(int32_t B, int32_t Hq, int3
   const DecodePlan p = plan_decode(B, Hkv, block_table_stride, page_size, num_splits);
   if (p.s_stride == 0) return 0;
   return partial_bytes(static_cast<long long>(B) * Hq, p.s_stride, nullptr);
+}
+
+ATTN_SINK_API size_t attn_sink_mixed_workspace_size(int32_t num_decode, int32_t Hq, int32_t Hkv,
+                                                    int32_t D, int32_t block_table_stride,
+                                                    int32_t page_size) {
+  if (num_decode < 0 || Hq <= 0 || Hkv <= 0 || D != kHeadDim || block_table_stride <= 0 ||
+      page_size <= 0)
+    return 0;
+  const int s_stride = mixed_slots(block_table_stride, page_size);
+  return kPrefillWorkspaceBytes +
+         (s_stride > 1 ? partial_bytes(static_cast<long long>(num_decode) * Hq, s_stride, nullptr) : 0);
 }
 
 ATTN_SINK_API size_t attn_sink_prefill_workspace_size(int32_t B, int32_t Hq, int32_t D,
@@ -378,7 +396,137 @@ attn_sink_status decode_impl(
     m.kv_lens = kv_lens;
     m.Hq = Hq;
     m.chunk_units = p.chunk_units;
+    m.kv_cap = block_table_stride * page_size;  // as the split kernel clamps kv_len
   }
+  return from_cuda(launch_merge(m, s));
+}
+
+// Ragged prefill (num_decode < 0) or a mixed batch whose first num_decode
+// sequences are single-query decode rows (attn_sink_mixed).
+attn_sink_status prefill_impl(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* kv_lens, const int32_t* block_table, int32_t block_table_stride,
+    const float* sinks, void* out, float* lse, int32_t B, int32_t num_decode, int32_t total_q,
+    int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+    float scale, int32_t causal, attn_sink_dtype dtype, int32_t* err_flag, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  const bool mixed = num_decode >= 0;
+  attn_sink_status st =
+      check_shapes(B, Hq, Hkv, D, page_size, num_pages, block_table_stride, dtype);
+  if (st != ATTN_SINK_OK) return st;
+  if (!q || !k_cache || !v_cache || !cu_seqlens_q || !kv_lens || !block_table || !sinks || !out)
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (total_q < 0 || max_q_len < 0 || (causal != 0 && causal != 1) || !std::isfinite(scale))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (mixed && dtype == ATTN_SINK_BF16 && (B > kMixedMaxSeqs || Hq > kMixedMaxHeads))
+    return ATTN_SINK_ERR_UNSUPPORTED;
+  if (B == 0 || total_q == 0) return ATTN_SINK_OK;
+  if (max_q_len == 0 && !(mixed && num_decode > 0)) return ATTN_SINK_OK;
+  if (static_cast<long long>(total_q) * Hq > INT_MAX) return ATTN_SINK_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int group = Hq / Hkv;
+
+  if (dtype == ATTN_SINK_FP32) {
+    // fp32 runs the whole batch (decode rows included) on the SIMT path.
+    SimtArgs a{};
+    a.q = static_cast<const float*>(q);
+    a.k_cache = static_cast<const float*>(k_cache);
+    a.v_cache = static_cast<const float*>(v_cache);
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.kv_lens = kv_lens;
+    a.block_table = block_table;
+    a.sinks = sinks;
+    a.out = static_cast<float*>(out);
+    a.lse = lse;
+    a.err_flag = err_flag;
+    a.B = B;
+    a.total_q = total_q;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.group = group;
+    a.bt_stride = block_table_stride;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    a.scale_log2 = scale * kLog2e;
+    a.causal = causal;
+    a.num_splits = 1;
+    return from_cuda(launch_simt_fp32(a, s));
+  }
+
+  const int s_stride = mixed ? mixed_slots(block_table_stride, page_size) : 0;
+  const size_t need = mixed ? attn_sink_mixed_workspace_size(num_decode, Hq, Hkv, D,
+                                                             block_table_stride, page_size)
+                            : kPrefillWorkspaceBytes;
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_SINK_ERR_WORKSPACE;
+  CUtensorMap q_map, k_map, v_map, k8_map, v8_map;
+  const uint64_t rows = static_cast<uint64_t>(num_pages) * page_size;
+  if (!make_map_q(&q_map, q, static_cast<uint64_t>(total_q), static_cast<uint64_t>(Hq),
+                  static_cast<uint32_t>(group), static_cast<uint32_t>(128 / group)) ||
+      !make_map_2d(&k_map, k_cache, static_cast<uint64_t>(Hkv) * kHeadDim, rows, kUnitTokens) ||
+      !make_map_2d(&v_map, v_cache, static_cast<uint64_t>(Hkv) * kHeadDim, rows, kUnitTokens))
+    return ATTN_SINK_ERR_CUDA;
+  if (mixed &&
+      (!make_map_paged_heads(&k8_map, k_cache, static_cast<uint64_t>(num_pages),
+                             static_cast<uint64_t>(page_size), static_cast<uint64_t>(Hkv), kMixedBoxHeads) ||
+       !make_map_paged_heads(&v8_map, v_cache, static_cast<uint64_t>(num_pages),
+                             static_cast<uint64_t>(page_size), static_cast<uint64_t>(Hkv), kMixedBoxHeads)))
+    return ATTN_SINK_ERR_CUDA;
+  PrefillArgs a{};
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.kv_lens = kv_lens;
+  a.block_table = block_table;
+  a.sinks = sinks;
+  a.out = out;
+  a.lse = lse;
+  a.err_flag = err_flag;
+  a.B = B;
+  a.total_q = total_q;
+  a.max_q_len = max_q_len;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.group = group;
+  a.bt_stride = block_table_stride;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal;
+  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  a.tile_ctr = static_cast<unsigned long long*>(workspace);
+  if (!mixed) return from_cuda(launch_prefill_bf16(a, q_map, k_map, v_map, s));
+
+  MixedArgs mx{};
+  mx.num_decode = num_decode;
+  mx.q = q;
+  mx.dec_ctr = a.tile_ctr + 1;
+  mx.dec_chunk_units = kMixedChunkUnits;
+  size_t o_bytes = 0;
+  if (s_stride > 1) {
+    partial_bytes(static_cast<long long>(num_decode) * Hq, s_stride, &o_bytes);
+    char* parts = static_cast<char*>(workspace) + kPrefillWorkspaceBytes;
+    mx.o_part = reinterpret_cast<float*>(parts);
+    mx.lse_part = reinterpret_cast<float*>(parts + o_bytes);
+    mx.s_stride = s_stride;
+  }
+  cudaError_t e = launch_mixed_bf16(a, mx, q_map, k_map, v_map, k8_map, v8_map, s);
+  if (e != cudaSuccess || s_stride <= 1 || num_decode == 0) return from_cuda(e);
+  // Decode rows split into several items: LSE merge of their partials.
+  MergeArgs m{};
+  m.o_part = mx.o_part;
+  m.lse_part = mx.lse_part;
+  m.out = out;
+  m.lse = lse;
+  m.rows = num_decode * Hq;
+  m.s_stride = s_stride;
+  m.num_parts = s_stride;
+  m.out_fp32 = 0;
+  m.kv_lens = kv_lens;
+  m.Hq = Hq;
+  m.chunk_units = kMixedChunkUnits;
+  m.kv_cap = block_table_stride * page_size;
+  m.seq_start = cu_seqlens_q;
   return from_cuda(launch_merge(m, s));
 }
 
@@ -437,78 +585,22 @@ ATTN_SINK_API attn_sink_status attn_sink_prefill(
     int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages, float scale,
     int32_t causal, attn_sink_dtype dtype, int32_t* err_flag, void* workspace,
     size_t workspace_bytes, void* stream) {
-  attn_sink_status st =
-      check_shapes(B, Hq, Hkv, D, page_size, num_pages, block_table_stride, dtype);
-  if (st != ATTN_SINK_OK) return st;
-  if (!q || !k_cache || !v_cache || !cu_seqlens_q || !kv_lens || !block_table || !sinks || !out)
-    return ATTN_SINK_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-    return ATTN_SINK_ERR_INVALID_ARG;
-  if (total_q < 0 || max_q_len < 0 || (causal != 0 && causal != 1) || !std::isfinite(scale))
-    return ATTN_SINK_ERR_INVALID_ARG;
-  if (B == 0 || total_q == 0 || max_q_len == 0) return ATTN_SINK_OK;
-  if (static_cast<long long>(total_q) * Hq > INT_MAX) return ATTN_SINK_ERR_UNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int group = Hq / Hkv;
+  return prefill_impl(q, k_cache, v_cache, cu_seqlens_q, kv_lens, block_table, block_table_stride,
+                      sinks, out, lse, B, -1, total_q, max_q_len, Hq, Hkv, D, page_size, num_pages,
+                      scale, causal, dtype, err_flag, workspace, workspace_bytes, stream);
+}
 
-  if (dtype == ATTN_SINK_FP32) {
-    SimtArgs a{};
-    a.q = static_cast<const float*>(q);
-    a.k_cache = static_cast<const float*>(k_cache);
-    a.v_cache = static_cast<const float*>(v_cache);
-    a.cu_seqlens_q = cu_seqlens_q;
-    a.kv_lens = kv_lens;
-    a.block_table = block_table;
-    a.sinks = sinks;
-    a.out = static_cast<float*>(out);
-    a.lse = lse;
-    a.err_flag = err_flag;
-    a.B = B;
-    a.total_q = total_q;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.group = group;
-    a.bt_stride = block_table_stride;
-    a.page_size = page_size;
-    a.num_pages = num_pages;
-    a.scale_log2 = scale * kLog2e;
-    a.causal = causal;
-    a.num_splits = 1;
-    return from_cuda(launch_simt_fp32(a, s));
-  }
-
-  if (!workspace || workspace_bytes < kPrefillWorkspaceBytes ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return ATTN_SINK_ERR_WORKSPACE;
-  CUtensorMap q_map, k_map, v_map;
-  const uint64_t rows = static_cast<uint64_t>(num_pages) * page_size;
-  if (!make_map_q(&q_map, q, static_cast<uint64_t>(total_q), static_cast<uint64_t>(Hq),
-                  static_cast<uint32_t>(group), static_cast<uint32_t>(128 / group)) ||
-      !make_map_2d(&k_map, k_cache, static_cast<uint64_t>(Hkv) * kHeadDim, rows, kUnitTokens) ||
-      !make_map_2d(&v_map, v_cache, static_cast<uint64_t>(Hkv) * kHeadDim, rows, kUnitTokens))
-    return ATTN_SINK_ERR_CUDA;
-  PrefillArgs a{};
-  a.cu_seqlens_q = cu_seqlens_q;
-  a.kv_lens = kv_lens;
-  a.block_table = block_table;
-  a.sinks = sinks;
-  a.out = out;
-  a.lse = lse;
-  a.err_flag = err_flag;
-  a.B = B;
-  a.total_q = total_q;
-  a.max_q_len = max_q_len;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.group = group;
-  a.bt_stride = block_table_stride;
-  a.page_size = page_size;
-  a.num_pages = num_pages;
-  a.scale_log2 = scale * kLog2e;
-  a.causal = causal;
-  a.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-  a.tile_ctr = static_cast<unsigned long long*>(workspace);
-  return from_cuda(launch_prefill_bf16(a, q_map, k_map, v_map, s));
+ATTN_SINK_API attn_sink_status attn_sink_mixed(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+    const int32_t* kv_lens, const int32_t* block_table, int32_t block_table_stride,
+    const float* sinks, void* out, float* lse, int32_t B, int32_t num_decode, int32_t total_q,
+    int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+    float scale, int32_t causal, attn_sink_dtype dtype, int32_t* err_flag, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  if (num_decode < 0 || num_decode > B) return ATTN_SINK_ERR_INVALID_ARG;
+  return prefill_impl(q, k_cache, v_cache, cu_seqlens_q, kv_lens, block_table, block_table_stride,
+                      sinks, out, lse, B, num_decode, total_q, max_q_len, Hq, Hkv, D, page_size,
+                      num_pages, scale, causal, dtype, err_flag, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -30,11 +30,14 @@
 //
 // The kernel is HBM-bound: per key and KV head it moves 256 B and does
 // 2*G*64 MACs, which the tensor-core path hides completely.
+#include "decode_unit.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace attn_sink {
 namespace {
+
+using namespace dec;
 
 constexpr int kConsumerWarps = 4;
 constexpr int kStages = 4;
@@ -44,8 +47,6 @@ constexpr int kHalfBytes = kHeadsPerCta * kUnitBytes;               // 8 KB: one
 constexpr int kStageBytes = 2 * kHalfBytes;                          // 16 KB (K then V)
 constexpr int kRingBytes = kStages * kStageBytes;                    // 64 KB
 constexpr int kSmemBytes = kRingBytes + 1024 /*align slack*/ + 128 /*barriers*/;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 struct alignas(8) Barriers {
   uint64_t full[kStages];
@@ -54,151 +55,6 @@ struct alignas(8) Barriers {
   int abort_word;
 };
 static_assert(kConsumerWarps == kHeadsPerCta, "one consumer warp per KV head of the CTA");
-
-__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
-                                        uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3, uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Byte offset of 16-byte chunk `chunk` of row `row` in a 128B-swizzled tile
-// whose base is 1024-byte aligned (the layout TMA writes with SWIZZLE_128B).
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-// Keep the bf16 halves of a B fragment whose key index is below n_valid.
-__device__ __forceinline__ uint32_t mask_keys(uint32_t v, int key_lo, int n_valid) {
-  uint32_t keep = (key_lo < n_valid ? 0x0000FFFFu : 0u) | (key_lo + 1 < n_valid ? 0xFFFF0000u : 0u);
-  return v & keep;
-}
-
-// Online-softmax state of one consumer warp for rows r0 = lane/4 and r1 = r0+8.
-struct WarpState {
-  float m0, m1;   // running max, log2 domain (quad-uniform)
-  float d0, d1;   // this thread's share of the running sum of exact p (for lse)
-  float w0, w1;   // the same over the bf16-rounded p fed to P*V (normalises O)
-  float o[8][4];  // O fragments: [d tile][c0..c3]
-};
-
-// One 16-key unit: S = Q K^T, online softmax update, O += P V.
-template <bool kTwoRows>
-__device__ __forceinline__ void consume_unit(uint32_t k_base, uint32_t v_base, int n_valid,
-                                             const uint32_t (&qa)[4][4], float scale_log2,
-                                             WarpState& st) {
-  const int lane = threadIdx.x & 31;
-  float s[2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
-
-  {
-    const int mi = lane >> 3, ri = lane & 7;
-    const int key = (mi >> 1) * 8 + ri;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      uint32_t b00, b01, b10, b11;
-      ldsm_x4(b00, b01, b10, b11, k_base + swz(key, 2 * ks + (mi & 1)));
-      mma_16816(s[0], qa[ks], b00, b01);
-      mma_16816(s[1], qa[ks], b10, b11);
-    }
-  }
-
-  const int kc = 2 * (lane & 3);
-  float x[2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int key = nt * 8 + kc + (e & 1);
-      const bool row_ok = kTwoRows || e < 2;
-      x[nt][e] = (key < n_valid && row_ok) ? s[nt][e] * scale_log2 : -INFINITY;
-    }
-
-  float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-  const float mn0 = fmaxf(st.m0, mx0);
-  const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-  const float al0 = fast_exp2(st.m0 - mu0);
-  st.m0 = mn0;
-
-  float mn1 = -INFINITY, mu1 = 0.f, al1 = 1.f;
-  if (kTwoRows) {
-    float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    mn1 = fmaxf(st.m1, mx1);
-    mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    al1 = fast_exp2(st.m1 - mu1);
-    st.m1 = mn1;
-  }
-
-  float p[2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    p[nt][0] = fast_exp2(x[nt][0] - mu0);
-    p[nt][1] = fast_exp2(x[nt][1] - mu0);
-    p[nt][2] = kTwoRows ? fast_exp2(x[nt][2] - mu1) : 0.f;
-    p[nt][3] = kTwoRows ? fast_exp2(x[nt][3] - mu1) : 0.f;
-  }
-  // P is rounded to bf16 for the P*V MMA.  w sums the same rounded values (so a
-  // row's weights sum to exactly 1); d sums the exact ones (for the lse).
-  uint32_t pa[4];
-  pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-  pa[1] = kTwoRows ? pack_bf16x2(p[0][2], p[0][3]) : 0u;
-  pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-  pa[3] = kTwoRows ? pack_bf16x2(p[1][2], p[1][3]) : 0u;
-  st.d0 = st.d0 * al0 + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-  st.w0 = st.w0 * al0 + (bf16_lo(pa[0]) + bf16_hi(pa[0])) + (bf16_lo(pa[2]) + bf16_hi(pa[2]));
-  if (kTwoRows) {
-    st.d1 = st.d1 * al1 + (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
-    st.w1 = st.w1 * al1 + (bf16_lo(pa[1]) + bf16_hi(pa[1])) + (bf16_lo(pa[3]) + bf16_hi(pa[3]));
-  }
-#pragma unroll
-  for (int dn = 0; dn < 8; ++dn) {
-    st.o[dn][0] *= al0;
-    st.o[dn][1] *= al0;
-    if (kTwoRows) {
-      st.o[dn][2] *= al1;
-      st.o[dn][3] *= al1;
-    }
-  }
-
-  const int mi = lane >> 3, ri = lane & 7;
-  const int vkey = (mi & 1) * 8 + ri;
-#pragma unroll
-  for (int dp = 0; dp < 4; ++dp) {
-    uint32_t v0, v1, v2, v3;
-    ldsm_x4_trans(v0, v1, v2, v3, v_base + swz(vkey, 2 * dp + (mi >> 1)));
-    if (n_valid < kUnitTokens) {  // unused slots of a last page may hold anything
-      v0 = mask_keys(v0, kc, n_valid);
-      v1 = mask_keys(v1, 8 + kc, n_valid);
-      v2 = mask_keys(v2, kc, n_valid);
-      v3 = mask_keys(v3, 8 + kc, n_valid);
-    }
-    mma_16816(st.o[2 * dp], pa, v0, v1);
-    mma_16816(st.o[2 * dp + 1], pa, v2, v3);
-  }
-}
 
 // kPoll: the waits poll (a test's short wait limit); otherwise they block.
 template <bool kTwoRows, bool kPoll>
@@ -343,36 +199,11 @@ __global__ void __launch_bounds__(kThreads)
   const int r0 = lane >> 2, r1 = r0 + 8;
   const int head0 = g * a.group;
   uint32_t qa[4][4];
-  {
-    const __nv_bfloat16* qb =
-        reinterpret_cast<const __nv_bfloat16*>(a.q) + (static_cast<long long>(b) * a.Hq + head0) * kHeadDim;
-    const int col = 2 * (lane & 3);
-    const bool ok0 = head_ok && r0 < a.group, ok1 = head_ok && r1 < a.group;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const int d = 16 * ks + col;
-      qa[ks][0] = ok0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * kHeadDim + d) : 0u;
-      qa[ks][1] = ok1 ? *reinterpret_cast<const uint32_t*>(qb + r1 * kHeadDim + d) : 0u;
-      qa[ks][2] = ok0 ? *reinterpret_cast<const uint32_t*>(qb + r0 * kHeadDim + d + 8) : 0u;
-      qa[ks][3] = ok1 ? *reinterpret_cast<const uint32_t*>(qb + r1 * kHeadDim + d + 8) : 0u;
-    }
-  }
-
+  load_q_frags(qa, reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                       (static_cast<long long>(b) * a.Hq + head0) * kHeadDim,
+               a.group, head_ok);
   WarpState st;
-  st.m0 = st.m1 = -INFINITY;
-  st.d0 = st.d1 = st.w0 = st.w1 = 0.f;
-#pragma unroll
-  for (int dn = 0; dn < 8; ++dn)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) st.o[dn][e] = 0.f;
-  if (c == 0 && head_ok) {
-    // The sink enters as the initial running max with running sum 1, in the
-    // first chunk only (one quad lane carries the 1).
-    st.m0 = r0 < a.group ? a.sinks[head0 + r0] * kLog2e : -INFINITY;
-    st.m1 = r1 < a.group ? a.sinks[head0 + r1] * kLog2e : -INFINITY;
-    st.d0 = st.w0 = (lane & 3) == 0 ? 1.f : 0.f;
-    st.d1 = st.w1 = (lane & 3) == 0 ? 1.f : 0.f;
-  }
+  init_state(st, a.sinks + head0, a.group, c == 0 && head_ok);
 
   for (int it = 0; it < n_iters; ++it) {
     const int stage = it % kStages;
@@ -392,41 +223,19 @@ __global__ void __launch_bounds__(kThreads)
   if (!head_ok) return;
 
   // ---- this warp holds its head's whole state: reduce the quad's sums, write
-  st.d0 += __shfl_xor_sync(0xffffffffu, st.d0, 1);
-  st.d0 += __shfl_xor_sync(0xffffffffu, st.d0, 2);
-  st.d1 += __shfl_xor_sync(0xffffffffu, st.d1, 1);
-  st.d1 += __shfl_xor_sync(0xffffffffu, st.d1, 2);
-  st.w0 += __shfl_xor_sync(0xffffffffu, st.w0, 1);
-  st.w0 += __shfl_xor_sync(0xffffffffu, st.w0, 2);
-  st.w1 += __shfl_xor_sync(0xffffffffu, st.w1, 1);
-  st.w1 += __shfl_xor_sync(0xffffffffu, st.w1, 2);
+  reduce_sums(st);
   const bool direct = n_chunks == 1;
-  const int col = 2 * (lane & 3);
 #pragma unroll
   for (int half = 0; half < (kTwoRows ? 2 : 1); ++half) {
     const int row = half ? r1 : r0;
     if (row >= a.group) continue;
-    const float m = half ? st.m1 : st.m0;
-    const float den = half ? st.d1 : st.d0;
-    const float wden = half ? st.w1 : st.w0;
-    const float inv = wden > 0.f ? 1.f / wden : 0.f;
-    const float lse = (den > 0.f && m != -INFINITY) ? (m + __log2f(den)) * kLn2 : -INFINITY;
     const long long grow = static_cast<long long>(b) * a.Hq + head0 + row;
-    if (direct) {
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim;
-#pragma unroll
-      for (int dn = 0; dn < 8; ++dn)
-        *reinterpret_cast<uint32_t*>(orow + dn * 8 + col) =
-            pack_bf16x2(st.o[dn][2 * half] * inv, st.o[dn][2 * half + 1] * inv);
-      if (a.lse && (lane & 3) == 0) a.lse[grow] = lse;
-    } else {
-      float* prow = a.o_part + (grow * a.s_stride + c) * kHeadDim;
-#pragma unroll
-      for (int dn = 0; dn < 8; ++dn)
-        *reinterpret_cast<float2*>(prow + dn * 8 + col) =
-            make_float2(st.o[dn][2 * half] * inv, st.o[dn][2 * half + 1] * inv);
-      if ((lane & 3) == 0) a.lse_part[grow * a.s_stride + c] = lse;
-    }
+    if (direct)
+      write_row(st, half, reinterpret_cast<__nv_bfloat16*>(a.out) + grow * kHeadDim,
+                a.lse ? a.lse + grow : nullptr, nullptr, nullptr);
+    else
+      write_row(st, half, nullptr, nullptr, a.o_part + (grow * a.s_stride + c) * kHeadDim,
+                a.lse_part + grow * a.s_stride + c);
   }
 }
 

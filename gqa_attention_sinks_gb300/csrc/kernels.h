@@ -87,6 +87,10 @@ struct MergeArgs {
   // written by the decode kernel and are skipped.
   const int32_t* kv_lens;
   int Hq, chunk_units;
+  int kv_cap;                  // keys beyond this are not read (0: no cap)
+  // When set, row r = b * Hq + h writes output row seq_start[b] * Hq + h (the
+  // decode rows of a ragged batch).
+  const int32_t* seq_start;
 };
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
@@ -131,11 +135,38 @@ struct PrefillArgs {
   unsigned long long* tile_ctr;  // work-tile claim counter (workspace), zeroed before launch
 };
 
-// Bytes of workspace the bf16 prefill uses (its work-tile claim counter).
+// What the mixed kernel adds (attn_sink_mixed): sequences [0, num_decode) hold
+// one query each and run as split-KV decode items instead of query tiles.
+// (A separate kernel parameter: growing PrefillArgs measurably changed the
+// register allocation, and the speed, of the plain prefill kernel.)
+struct MixedArgs {
+  int num_decode;
+  const void* q;               // bf16 [total_q, Hq, 64]: the decode rows' queries
+  unsigned long long* dec_ctr; // decode-item claim counter (workspace), zeroed before launch
+  int dec_chunk_units;         // 16-key units per decode item
+  float* o_part;               // fp32 [num_decode*Hq, s_stride, 64] decode partials
+  float* lse_part;             // fp32 [num_decode*Hq, s_stride]
+  int s_stride;                // partial slots per decode row (<= 1: every decode row is unsplit)
+};
+
+// Bytes of workspace the bf16 prefill uses (its work-tile claim counter); the
+// mixed kernel keeps its decode-item counter in the same block.
 constexpr size_t kPrefillWorkspaceBytes = 256;
+// Keys per decode item of a mixed batch: 1024 keys of 8 KV heads (2 MB of K/V).
+constexpr int kMixedChunkUnits = 64;
+constexpr int kMixedBoxHeads = 8;       // KV heads per decode-item TMA box
+// The mixed kernel keeps sequence lengths and sinks in shared memory.
+constexpr int kMixedMaxSeqs = 1024, kMixedMaxHeads = 256;
 
 cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
                                 const CUtensorMap& k_map, const CUtensorMap& v_map,
                                 cudaStream_t stream);
+
+// The mixed kernel: the prefill kernel with decode items; k8_map / v8_map view
+// the caches as 4-D tensors with boxes of 16 keys x 8 KV heads.
+cudaError_t launch_mixed_bf16(const PrefillArgs& a, const MixedArgs& mx, const CUtensorMap& q_map,
+                              const CUtensorMap& k_map, const CUtensorMap& v_map,
+                              const CUtensorMap& k8_map, const CUtensorMap& v8_map,
+                              cudaStream_t stream);
 
 }  // namespace attn_sink

@@ -31,11 +31,14 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const MergeArgs a) {
 
   int n = a.num_parts;
   if (a.kv_lens) {
-    const int kv = max(0, a.kv_lens[row / a.Hq]);
+    int kv = max(0, a.kv_lens[row / a.Hq]);
+    if (a.kv_cap > 0) kv = min(kv, a.kv_cap);
     const int units = (kv + kUnitTokens - 1) / kUnitTokens;
     n = max(1, (units + a.chunk_units - 1) / a.chunk_units);
     if (n == 1) return;  // the decode kernel wrote this row directly
     n = min(n, a.s_stride);
+    // a ragged batch's decode sequence without a query row has no output row
+    if (a.seq_start && a.seq_start[row / a.Hq + 1] <= a.seq_start[row / a.Hq]) return;
   }
   const float* lse_row = a.lse_part + static_cast<long long>(row) * a.s_stride;
   const float* o_row = a.o_part + static_cast<long long>(row) * a.s_stride * kHeadDim;
@@ -71,14 +74,16 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const MergeArgs a) {
   const float inv = den > 0.f ? 1.f / den : 0.f;
   acc.x *= inv;
   acc.y *= inv;
-  const long long base = static_cast<long long>(row) * kHeadDim + 2 * lane;
+  const long long orow = a.seq_start ? static_cast<long long>(a.seq_start[row / a.Hq]) * a.Hq + row % a.Hq
+                                     : static_cast<long long>(row);
+  const long long base = orow * kHeadDim + 2 * lane;
   if (a.out_fp32) {
     *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + base) = acc;
   } else {
     *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + base) =
         pack_bf16x2(acc.x, acc.y);
   }
-  if (a.lse && lane == 0) a.lse[row] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
+  if (a.lse && lane == 0) a.lse[orow] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
 }
 
 }  // namespace

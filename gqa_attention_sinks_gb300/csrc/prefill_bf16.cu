@@ -44,6 +44,7 @@
 // warpgroup hands S back (s_free) as soon as it has loaded it, so S(j+1) is
 // computed while the softmax of tile j runs.  Every barrier phase is counted
 // across work tiles, so the pipeline never drains between them.
+#include "decode_unit.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -86,13 +87,21 @@ constexpr int kOffKV = kQBufs * kQBufBytes;
 constexpr int kOffBar = kOffKV + kStages * kStageBytes;
 // Per-sequence lengths and per-head sinks are copied to shared memory when
 // they fit, so that decoding a work tile costs no global-memory round trip.
-constexpr int kMetaSeqs = 1024, kMetaHeads = 256;
+constexpr int kMetaSeqs = kMixedMaxSeqs, kMetaHeads = kMixedMaxHeads;
 constexpr int kBarBytes = 512;
 constexpr int kOffMeta = kOffBar + kBarBytes;
 constexpr int kMetaBytes = ((2 * kMetaSeqs + 1 + kMetaHeads) * 4 + 255) / 256 * 256;
 constexpr int kOffSort = kOffMeta + kMetaBytes;
-constexpr int kSortBytes = 2048 * 4 + 256;  // the sorted query blocks and their counter
-constexpr int kSmemBytes = kOffSort + kSortBytes + 1024;
+constexpr int kSortBytes = 2048 * 4;        // the sorted query blocks
+constexpr int kOffSched = kOffSort + kSortBytes;
+constexpr int kSchedBytes = 256;            // SchedInfo
+// Mixed batches: first decode item of every decode sequence (prefix sums).
+constexpr int kOffDecItems = kOffSched + kSchedBytes;
+constexpr int kDecItemsBytes = ((kMetaSeqs + 1) * 4 + 255) / 256 * 256;
+constexpr int kSmemBytes = kOffDecItems + kDecItemsBytes + 1024;
+// Decode items: KV heads per item (one consumer warp each, one TMA box).
+constexpr int kDecHeads = kMixedBoxHeads;
+constexpr int kDecHeadBytes = kUnitTokens * kHeadDim * 2;   // 2 KB: 16 keys of one head
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
@@ -154,13 +163,17 @@ __device__ __forceinline__ int block_key_tiles(const PrefillArgs& a, int q_len, 
 
 // Work tile t of the row-major list: t = r * (B * Hkv) + b * Hkv + g.
 // Returns false when sequence b has no query block r.
+template <bool kMixed = false>
 __device__ __forceinline__ bool decode_tile(const PrefillArgs& a, const Meta& m, long long t,
-                                            int tok_per_cta, WorkTile& w) {
+                                            int tok_per_cta, WorkTile& w, int num_decode = 0) {
   const long long heads = static_cast<long long>(a.B) * a.Hkv;
   const int r = static_cast<int>(t / heads);  // 0: last query block of each sequence
   const int rem = static_cast<int>(t % heads);
   w.b = rem / a.Hkv;
   w.g = rem % a.Hkv;
+  if constexpr (kMixed) {
+    if (w.b < num_decode) return false;  // a mixed batch's decode rows run as decode items
+  }
   w.q_start = m.cu_seqlens_q[w.b];
   w.q_len = m.cu_seqlens_q[w.b + 1] - w.q_start;
   const int n_blocks = w.q_len > 0 ? (w.q_len + tok_per_cta - 1) / tok_per_cta : 0;
@@ -184,12 +197,47 @@ __device__ __forceinline__ uint32_t block_sort_key(int cost, int r, int b) {
          static_cast<uint32_t>(b);
 }
 
+// Scheduling facts every CTA derives identically at launch.
+struct SchedInfo {
+  int sort_count;                 // query blocks placed in the sorted list
+  int n_dec_items;                // decode items of a mixed batch
+  int dec_first_ctas;             // CTAs that claim decode items before query tiles
+  int pad;
+  unsigned long long key_tiles;   // query-block key tiles (x Hkv: work of the query tiles)
+  unsigned long long dec_units;   // decode units (16 keys x Hkv heads each)
+};
+
 // Builds the sorted list in shared memory (all threads of the CTA).  Every
 // CTA builds the same list: the keys are distinct, so their sorted order does
 // not depend on where each thread placed them.  Returns the number of query
 // blocks, or -1 when the list is not used: all sequences alike (the row-major
 // list is then already in cost order), more than kSortMax blocks, or the
 // metadata is not in shared memory.
+// Pads keys[n..) to a power of two and sorts them ascending (bitonic; all
+// threads of the CTA).
+__device__ __forceinline__ void sort_keys_ascending(uint32_t* keys, int n) {
+  int pow2 = 1;
+  while (pow2 < n) pow2 <<= 1;
+  for (int i = n + threadIdx.x; i < pow2; i += blockDim.x) keys[i] = 0xFFFFFFFFu;
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int k = 2; k <= pow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint32_t x = keys[i], y = keys[l];
+          if (((i & k) == 0) == (x > y)) {
+            keys[i] = y;
+            keys[l] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 __device__ __forceinline__ int build_sorted_blocks(const PrefillArgs& a, const Meta& m, bool meta_in_smem,
                                    int tok_per_cta, uint32_t* keys, int* counter) {
   if (!meta_in_smem || a.B > 1024) return -1;
@@ -237,13 +285,119 @@ __device__ __forceinline__ int build_sorted_blocks(const PrefillArgs& a, const M
   return n;
 }
 
+// The same for a mixed batch (query tiles of sequences [num_decode, B) only,
+// always sorted), also summing the query tiles' key tiles.  The SchedInfo
+// fields are zero on entry.
+__device__ __forceinline__ int build_sorted_blocks_mixed(const PrefillArgs& a, const MixedArgs& mx,
+                                                         const Meta& m, int tok_per_cta, uint32_t* keys,
+                                                         SchedInfo* info) {
+  unsigned long long tiles = 0;
+  for (int b = mx.num_decode + threadIdx.x; b < a.B; b += blockDim.x) {
+    const int q_len = m.cu_seqlens_q[b + 1] - m.cu_seqlens_q[b];
+    const int n_blocks = q_len > 0 ? (q_len + tok_per_cta - 1) / tok_per_cta : 0;
+    const int kv_len = min(max(0, m.kv_lens[b]), a.bt_stride * a.page_size);
+    for (int r = 0; r < n_blocks; ++r) {
+      int tok0;
+      const int cost = block_key_tiles(a, q_len, kv_len, n_blocks, r, tok_per_cta, tok0);
+      tiles += static_cast<unsigned long long>(cost);
+      const int slot = atomicAdd(&info->sort_count, 1);
+      if (slot < kSortMax) keys[slot] = block_sort_key(cost, r, b);
+    }
+  }
+  atomicAdd(&info->key_tiles, tiles);
+  __syncthreads();
+  const int n = info->sort_count;
+  if (n > kSortMax) return -1;
+  sort_keys_ascending(keys, n);
+  return n;
+}
+
+// ---------------------------------------------------------------- decode items
+// A mixed batch's decode sequence b (one query at position kv_len - 1, which
+// sees every key) runs as decode items: chunk c of kMixedChunkUnits 16-key
+// units x a group of kDecHeads KV heads.  Sequence b's items are numbered from
+// item_start[b], chunk-major (head group fastest).
+struct DecItem {
+  int b, hg, c, n_chunks, u0, u1, kv_len;
+};
+
+__device__ __forceinline__ int m_kv_raw(const Meta& m, int b) { return max(0, m.kv_lens[b]); }
+
+// Key length of decode sequence b as the kernel reads it, and its chunks.
+__device__ __forceinline__ int dec_kv_len(const PrefillArgs& a, const Meta& m, int b) {
+  return min(max(0, m.kv_lens[b]), a.bt_stride * a.page_size);
+}
+__device__ __forceinline__ int dec_chunks(const MixedArgs& mx, int kv_len) {
+  const int units = (kv_len + kUnitTokens - 1) / kUnitTokens;
+  return max(1, (units + mx.dec_chunk_units - 1) / mx.dec_chunk_units);
+}
+
+// Fills item_start[0..num_decode] (all threads of the CTA) and the decode work.
+__device__ __forceinline__ void build_decode_items(const PrefillArgs& a, const MixedArgs& mx, const Meta& m,
+                                                   int* item_start, SchedInfo* info) {
+  const int n_hg = (a.Hkv + kDecHeads - 1) / kDecHeads;
+  unsigned long long units = 0;
+  for (int b = threadIdx.x; b < mx.num_decode; b += blockDim.x) {
+    const int kv = dec_kv_len(a, m, b);
+    item_start[b + 1] = dec_chunks(mx, kv) * n_hg;
+    units += static_cast<unsigned long long>((kv + kUnitTokens - 1) / kUnitTokens);
+  }
+  atomicAdd(&info->dec_units, units);
+  if (threadIdx.x == 0) item_start[0] = 0;
+  __syncthreads();
+  // inclusive scan of item_start[1..num_decode] by warp 0: lane l sums a
+  // contiguous run, then the runs' totals are scanned across the warp
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (mx.num_decode + 31) / 32;
+    const int lo = 1 + lane * per, hi = min(mx.num_decode, lo + per - 1);
+    int run = 0;
+    for (int i = lo; i <= hi; ++i) run += item_start[i];
+    int incl = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += x;
+    }
+    int acc = incl - run;
+    for (int i = lo; i <= hi; ++i) {
+      acc += item_start[i];
+      item_start[i] = acc;
+    }
+    if (lane == 31) info->n_dec_items = incl;
+  }
+  __syncthreads();
+}
+
+// Decode item k: binary search of its sequence in item_start.
+__device__ __forceinline__ void decode_item(const PrefillArgs& a, const MixedArgs& mx, const Meta& m,
+                                            const int* item_start, int k, DecItem& d) {
+  int lo = 0, hi = mx.num_decode - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (item_start[mid] <= k) lo = mid; else hi = mid - 1;
+  }
+  const int n_hg = (a.Hkv + kDecHeads - 1) / kDecHeads;
+  const int within = k - item_start[lo];
+  d.b = lo;
+  d.hg = within % n_hg;
+  d.c = within / n_hg;
+  d.kv_len = dec_kv_len(a, m, lo);
+  d.n_chunks = dec_chunks(mx, d.kv_len);
+  const int units = (d.kv_len + kUnitTokens - 1) / kUnitTokens;
+  d.u0 = min(units, d.c * mx.dec_chunk_units);
+  d.u1 = min(units, d.u0 + mx.dec_chunk_units);
+}
+
 // Claims the next work tile (warp-collective; every lane returns the same
 // row-major tile index, or -1 when every tile has been claimed).  With the
 // sorted list (n_sorted >= 0) claim k is query block keys[k / Hkv], KV head
 // k % Hkv; without it the claims walk the row-major list and pass over the
 // indices past a sequence's last block.
+template <bool kMixed = false>
 __device__ __forceinline__ long long claim_tile(const PrefillArgs& a, const Meta& m, long long n_tiles,
-                                                int tok_per_cta, const uint32_t* keys, int n_sorted) {
+                                                int tok_per_cta, const uint32_t* keys, int n_sorted,
+                                                int num_decode = 0) {
   const int lane = threadIdx.x & 31;
   const long long n_claims = n_sorted >= 0 ? static_cast<long long>(n_sorted) * a.Hkv : n_tiles;
   for (;;) {
@@ -257,8 +411,47 @@ __device__ __forceinline__ long long claim_tile(const PrefillArgs& a, const Meta
       return static_cast<long long>(r) * a.B * a.Hkv + static_cast<long long>(b) * a.Hkv + k % a.Hkv;
     }
     WorkTile w;
-    if (decode_tile(a, m, k, tok_per_cta, w)) return k;
+    if (decode_tile<kMixed>(a, m, k, tok_per_cta, w, num_decode)) return k;
   }
+}
+
+// Tile indices handed through the ring: >= 0 a query tile (row-major index),
+// -1 no work left, <= -2 decode item -2 - index.
+__device__ __forceinline__ bool is_decode_item(long long t) { return t <= -2; }
+__device__ __forceinline__ int decode_item_index(long long t) { return static_cast<int>(-2 - t); }
+
+// The claiming warp's view of the two queues of a mixed batch.
+struct Claimer {
+  bool tiles_done = false, items_done = false;
+};
+
+// Next piece of work for this CTA (warp-collective).  CTAs below
+// dec_first_ctas take decode items first, the others query tiles first; each
+// turns to the other queue when its own runs dry, so HBM-bound decode items
+// and tensor-bound query tiles run on different SMs at the same time.
+template <bool kMixed>
+__device__ __forceinline__ long long claim_work(const PrefillArgs& a, const MixedArgs& mx, const Meta& m,
+                                                long long n_tiles, int tok_per_cta, const uint32_t* keys,
+                                                int n_sorted, const SchedInfo* info, Claimer& cl) {
+  const int lane = threadIdx.x & 31;
+  const bool items_first = kMixed && static_cast<int>(blockIdx.x) < info->dec_first_ctas;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool items = kMixed && (pass == 0) == items_first;
+    if (items) {
+      if (cl.items_done) continue;
+      unsigned long long c = 0;
+      if (lane == 0) c = atomicAdd(mx.dec_ctr, 1ull);
+      const long long k = static_cast<long long>(__shfl_sync(0xffffffffu, c, 0));
+      if (k < info->n_dec_items) return -2 - k;
+      cl.items_done = true;
+    } else {
+      if (cl.tiles_done) continue;
+      const long long t = claim_tile<kMixed>(a, m, n_tiles, tok_per_cta, keys, n_sorted, mx.num_decode);
+      if (t >= 0) return t;
+      cl.tiles_done = true;
+    }
+  }
+  return -1;
 }
 
 // A reader role takes claimed tile number i from the ring (warp-collective).
@@ -276,13 +469,25 @@ __device__ __forceinline__ bool take_tile(Bars* bars, int i, long long& t, volat
   return true;
 }
 
+// HBM rate one CTA sustains on decode items (GB/s; measured 47-60 on GB300,
+// where the 4-stage ring of one CTA per SM bounds the bytes in flight): the
+// mixed kernel sends at most 6.5 TB/s / this many CTAs to decode items first.
+constexpr float kDecodeCtaGBs = 60.f;
+
 // kPoll: the waits poll (a test's short wait limit); otherwise they block.
-template <bool kPoll>
+// kMixed: sequences [0, num_decode) run as decode items (attn_sink_mixed).
+template <bool kPoll, bool kMixed>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
-                   const __grid_constant__ CUtensorMap v_map, const PrefillArgs a,
-                   const long long n_tiles) {
+                   const __grid_constant__ CUtensorMap v_map,
+                   const __grid_constant__ CUtensorMap k8_map,
+                   const __grid_constant__ CUtensorMap v8_map, const PrefillArgs a,
+                   const MixedArgs mx, const long long n_tiles) {
+  // Arrivals that release a K/V stage: the two P*V commits of a query tile
+  // (each issued kKvRelease times in the mixed kernel), or in the mixed kernel
+  // the eight consumer warps of a decode item.
+  constexpr int kKvRelease = kMixed ? kSoftmaxWarps / kQTiles : 1;
   const int tok_per_tile = kRows / a.group;
   const int tok_per_cta = kQTiles * tok_per_tile;
 
@@ -300,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->kv_full[s], 2);   // the K and the V producer
-      mbar_init(&bars->kv_empty[s], kQTiles);  // released by every Q tile's P*V
+      mbar_init(&bars->kv_empty[s], kQTiles * kKvRelease);  // every Q tile's P*V (or decode warp)
     }
     for (int q = 0; q < kQTiles; ++q) {
       mbar_init(&bars->s_full[q], 2);   // the MMA commit and the MMA leader's s_uok arrive
@@ -316,6 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->tile_empty[i], kTileReaders);   // one arrive per reader warp
     }
     bars->abort_word = 0;
+    if constexpr (kMixed) {
+      SchedInfo* si = reinterpret_cast<SchedInfo*>(base + kOffSched);
+      si->sort_count = 0;
+      si->n_dec_items = 0;
+      si->dec_first_ctas = 0;
+      si->key_tiles = 0;
+      si->dec_units = 0;
+    }
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -333,10 +546,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     meta = Meta{cu_s, kvl_s, sinks_s};
   }
   uint32_t* sort_keys = reinterpret_cast<uint32_t*>(base + kOffSort);
+  SchedInfo* info = reinterpret_cast<SchedInfo*>(base + kOffSched);
+  int* dec_start = reinterpret_cast<int*>(base + kOffDecItems);
   __syncthreads();  // the metadata is in place
-  const int n_sorted = build_sorted_blocks(a, meta, a.B <= kMetaSeqs && a.Hq <= kMetaHeads,
-                                           tok_per_cta, sort_keys,
-                                           reinterpret_cast<int*>(base + kOffSort + 2048 * 4));
+  int n_sorted;
+  if constexpr (kMixed) {
+    n_sorted = build_sorted_blocks_mixed(a, mx, meta, tok_per_cta, sort_keys, info);
+    build_decode_items(a, mx, meta, dec_start, info);
+    if (threadIdx.x == 0 && info->n_dec_items > 0) {
+      // How many CTAs start on decode items: the decode share of the work, at
+      // most what saturates HBM (the others start on query tiles).
+      const float dec_us = static_cast<float>(info->dec_units) * kUnitTokens * a.Hkv * 256.f / 6.5e6f;
+      const float tile_us = static_cast<float>(info->key_tiles) * a.Hkv * 1.15f / gridDim.x;
+      int k = static_cast<int>(gridDim.x * dec_us / (dec_us + tile_us) + 0.5f);
+      k = min(k, static_cast<int>(6500.f / kDecodeCtaGBs + 0.999f));
+      info->dec_first_ctas = info->key_tiles == 0 ? static_cast<int>(gridDim.x) : max(1, k);
+    }
+  } else {
+    n_sorted = build_sorted_blocks(a, meta, a.B <= kMetaSeqs && a.Hq <= kMetaHeads, tok_per_cta,
+                                   sort_keys, &info->sort_count);
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -354,16 +583,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       if (is_k) tma_prefetch_map(&q_map);
       tma_prefetch_map(kv_map);
+      if constexpr (kMixed) tma_prefetch_map(is_k ? &k8_map : &v8_map);
     }
     const uint64_t once = l2_policy_evict_first();   // each Q tile is read by one CTA
     const uint64_t reuse = l2_policy_evict_last();   // K/V tiles serve every later query block
     int qw = 0, kv_it = 0;
     bool ok = true;
+    Claimer claimer;
     for (int i = 0; ok; ++i) {
       long long t;
       if (is_k) {
         // Claim the next tile and publish it to the other roles.
-        t = claim_tile(a, meta, n_tiles, tok_per_cta, sort_keys, n_sorted);
+        if constexpr (kMixed)
+          t = claim_work<kMixed>(a, mx, meta, n_tiles, tok_per_cta, sort_keys, n_sorted, info, claimer);
+        else
+          t = claim_tile(a, meta, n_tiles, tok_per_cta, sort_keys, n_sorted);
         const int slot = i % kTileRing;
         if (i >= kTileRing) {
           const bool ready = mbar_wait<kPoll>(&bars->tile_empty[slot], ((i / kTileRing) + 1) & 1,
@@ -380,9 +614,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = take_tile<kPoll>(bars, i, t, abort_word, a);
         if (!ok) break;
       }
-      if (t < 0) break;
+      if constexpr (kMixed) {
+      if (t == -1) break;
+      if (is_decode_item(t)) {
+        // A decode item: per 16-key unit one box of 16 keys x kDecHeads KV
+        // heads of K (this warp) or V (the other producer) into the stage.
+        DecItem d;
+        decode_item(a, mx, meta, dec_start, decode_item_index(t), d);
+        const CUtensorMap* map8 = is_k ? &k8_map : &v8_map;
+        const int32_t* bt_row = a.block_table + static_cast<long long>(d.b) * a.bt_stride;
+        if (is_k && d.c == 0 && lane == 0 && a.err_flag && m_kv_raw(meta, d.b) > d.kv_len)
+          atomicOr(a.err_flag, kFlagBadPage);
+        const int upp = a.page_size / kUnitTokens;
+        // lane l holds the page of unit u0 + 32 * window + l
+        auto page_of = [&](int it0) {
+          const int u = d.u0 + it0 + lane;
+          return u < d.u1 ? bt_row[u / upp] : -1;
+        };
+        int cur_phys = page_of(0), nxt_phys = page_of(32);
+        for (int it = 0; it < d.u1 - d.u0; ++it, ++kv_it) {
+          if (it > 0 && (it & 31) == 0) {
+            cur_phys = nxt_phys;
+            nxt_phys = page_of(it + 32);
+          }
+          const int st = kv_it % kStages;
+          if (kv_it >= kStages) {
+            const bool ready = mbar_wait<kPoll>(&bars->kv_empty[st], ((kv_it / kStages) + 1) & 1,
+                                                abort_word, a.err_flag, a.wait_limit_ns);
+            ok = __all_sync(0xffffffffu, ready);
+            if (!ok) break;
+          }
+          const int phys = __shfl_sync(0xffffffffu, cur_phys, it & 31);
+          const int tok = ((d.u0 + it) % upp) * kUnitTokens;
+          const bool unit_ok = phys >= 0 && phys < a.num_pages;
+          if (lane == 0) {
+            if (is_k) {
+              bars->unit_ok[st] = unit_ok ? 1u : 0u;  // published by the arrive below
+              if (!unit_ok && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
+            }
+            mbar_arrive_expect_tx(&bars->kv_full[st], unit_ok ? kDecHeads * kDecHeadBytes : 0);
+            if (unit_ok)
+              tma_load_4d_hint(base + kOffKV + st * kStageBytes + kv_off, map8, &bars->kv_full[st], 0,
+                               tok, d.hg * kDecHeads, phys, once);
+          }
+          __syncwarp();
+        }
+        continue;
+      }
+      } else {
+        if (t < 0) break;
+      }
       WorkTile w;
-      decode_tile(a, meta, t, tok_per_cta, w);  // a claimed tile always holds query rows
+      decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);  // a claimed tile always holds query rows
       if (is_k && w.kv_len < w.kv_raw && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
       if (w.n_kv == 0) continue;
       if (is_k) {
@@ -483,7 +766,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kKeys / 16; ++kk)
           umma_ts(tmem_o, tmem_p + kk * 8, v_desc0 + st * kStageDesc + kk * 128, kIdescPV, acc || kk > 0);
         umma_commit(&bars->pv_done[q]);
-        umma_commit(&bars->kv_empty[st]);
+        if constexpr (kMixed) {
+#pragma unroll
+          for (int k = 0; k < kKvRelease; ++k) umma_commit(&bars->kv_empty[st]);
+        } else {
+          umma_commit(&bars->kv_empty[st]);
+        }
       }
       __syncwarp();
     };
@@ -495,9 +783,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; ok; ++i) {
       long long t;
       ok = take_tile<kPoll>(bars, i, t, abort_word, a);
-      if (!ok || t < 0) break;
+      if constexpr (kMixed) {
+        if (!ok || t == -1) break;
+        if (is_decode_item(t)) {  // its stages go to the softmax warps
+          DecItem d;
+          decode_item(a, mx, meta, dec_start, decode_item_index(t), d);
+          kv_it += d.u1 - d.u0;
+          continue;
+        }
+      } else {
+        if (!ok || t < 0) break;
+      }
       WorkTile w;
-      decode_tile(a, meta, t, tok_per_cta, w);
+      decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
       if (w.n_kv == 0) continue;
       const int qb = qw % kQBufs;
       // Q loaded, the first K/V tile in, and the previous S read out of TMEM.
@@ -553,16 +851,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one computes exponentials while the other loads S, reduces and stores P.
     // Warpgroup 1 hands warpgroup 0 the first turn.
     if (kQTiles > 1 && q == 1 && lane == 0) mbar_arrive(&bars->exp_turn[0]);
-    // Key tiles consumed so far: every S, P*V and stage this warpgroup has
-    // gone through (all three advance together).
-    int it = 0;
+    // Key tiles consumed so far: every S and P*V this warpgroup has gone
+    // through (it), and the K/V stages (kv_it: the same count, plus the
+    // decode items' units in the mixed kernel).
+    int it = 0, kv_it = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
       long long t;
       ok = take_tile<kPoll>(bars, i, t, abort_word, a);
-      if (!ok || t < 0) break;
+      if constexpr (kMixed) {
+      if (!ok || t == -1) break;
+      if (is_decode_item(t)) {
+        // ------------------------------------------------------ decode item
+        // Softmax warp w is the consumer of KV head hg * kDecHeads + w: the
+        // split-KV decode step on its 2 KB slice of each stage.
+        DecItem d;
+        decode_item(a, mx, meta, dec_start, decode_item_index(t), d);
+        const int g = d.hg * kDecHeads + warp;
+        const long long qrow = meta.cu_seqlens_q[d.b];  // the sequence's one query
+        // (a decode sequence without a query row has nothing to read or write)
+        const bool head_ok = g < a.Hkv && meta.cu_seqlens_q[d.b + 1] > qrow;
+        const int head0 = g * a.group;
+        uint32_t qa[4][4];
+        dec::load_q_frags(qa, reinterpret_cast<const __nv_bfloat16*>(mx.q) + (qrow * a.Hq + head0) * kHeadDim,
+                          a.group, head_ok);
+        dec::WarpState ds;
+        dec::init_state(ds, meta.sinks + head0, a.group, d.c == 0 && head_ok);
+        const int n_units = d.u1 - d.u0;
+        for (int j = 0; j < n_units; ++j) {
+          const int st = (kv_it + j) % kStages;
+          const bool ready = mbar_wait<kPoll>(&bars->kv_full[st], ((kv_it + j) / kStages) & 1, abort_word,
+                                              a.err_flag, a.wait_limit_ns);
+          ok = __all_sync(0xffffffffu, ready);
+          if (!ok) break;
+          if (head_ok && bars->unit_ok[st]) {
+            const uint32_t k_base = smem_addr(base + kOffKV + st * kStageBytes + warp * kDecHeadBytes);
+            const uint32_t v_base = k_base + kTileBytes;
+            const int n_valid = min(kUnitTokens, d.kv_len - (d.u0 + j) * kUnitTokens);
+            if (a.group > 8)
+              dec::consume_unit<true>(k_base, v_base, n_valid, qa, scale_log2, ds);
+            else
+              dec::consume_unit<false>(k_base, v_base, n_valid, qa, scale_log2, ds);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->kv_empty[st]);  // one of kSoftmaxWarps releases
+        }
+        if (!ok) break;
+        kv_it += n_units;
+        if (head_ok) {
+          dec::reduce_sums(ds);
+          const int r0 = lane >> 2;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int row = r0 + 8 * half;
+            if (row >= a.group) continue;
+            const long long prow = static_cast<long long>(d.b) * a.Hq + head0 + row;
+            const long long orow = qrow * a.Hq + head0 + row;
+            if (d.n_chunks == 1)
+              dec::write_row(ds, half, reinterpret_cast<__nv_bfloat16*>(a.out) + orow * kHeadDim,
+                             a.lse ? a.lse + orow : nullptr, nullptr, nullptr);
+            else
+              dec::write_row(ds, half, nullptr, nullptr, mx.o_part + (prow * mx.s_stride + d.c) * kHeadDim,
+                             mx.lse_part + prow * mx.s_stride + d.c);
+          }
+        }
+        continue;
+      }
+      } else {
+        if (!ok || t < 0) break;
+      }
       WorkTile w;
-      decode_tile(a, meta, t, tok_per_cta, w);
+      decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
       const int tok = w.tok0 + q * tok_per_tile + r / a.group;
       const int head = w.g * a.group + r % a.group;
       const bool row_valid = tok < w.q_len;
@@ -571,7 +930,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float d_run = 1.f;                     // ... with running sum e^0 = 1
       for (int j = 0; j < w.n_kv; ++j) {
         const int u = it + j;
-        const int st = u % kStages;
+        int st;
+        if constexpr (kMixed)
+          st = (kv_it + j) % kStages;
+        else
+          st = u % kStages;
         // s_full completes after the MMA warp saw the stage's kv_full: the
         // stage has landed, and s_uok holds its unit mask.
         const bool ready = mbar_wait<kPoll>(&bars->s_full[q], u & 1, abort_word, a.err_flag, a.wait_limit_ns);
@@ -790,6 +1153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           a.lse[grow] = (d_run > 0.f && m_run != -INFINITY) ? (m_run + __log2f(d_run)) * kLn2 : -INFINITY;
       }
       it += w.n_kv;
+      if constexpr (kMixed) kv_it += w.n_kv;
     }
   }
 
@@ -802,18 +1166,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
-                                const CUtensorMap& k_map, const CUtensorMap& v_map,
-                                cudaStream_t stream) {
-  const int tok_per_cta = kQTiles * (kRows / a.group);
-  const long long blocks = (a.max_q_len + tok_per_cta - 1) / tok_per_cta;
-  const long long n_tiles = blocks * a.B * a.Hkv;
-  if (n_tiles <= 0) return cudaSuccess;
+namespace {
+
+template <bool kMixed>
+cudaError_t launch_kernel(const PrefillArgs& a, const MixedArgs& mx, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                          const CUtensorMap& v_map, const CUtensorMap& k8_map,
+                          const CUtensorMap& v8_map, long long n_tiles, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  auto kern = a.wait_limit_ns < kPollLimitNs ? prefill_kernel<true> : prefill_kernel<false>;
+  auto kern = a.wait_limit_ns < kPollLimitNs ? prefill_kernel<true, kMixed> : prefill_kernel<false, kMixed>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // The register split inside the kernel assumes the launch allocation; a
@@ -823,13 +1186,38 @@ cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-  const unsigned grid = static_cast<unsigned>(n_tiles < sms ? n_tiles : sms);
-  // The claim counter starts at zero on every launch (a memset node when the
+  // A mixed batch's decode items are counted on the device: every SM gets a CTA.
+  const unsigned grid = static_cast<unsigned>(kMixed || n_tiles >= sms ? sms : n_tiles);
+  // The claim counters start at zero on every launch (a memset node when the
   // stream is being captured).
-  e = cudaMemsetAsync(a.tile_ctr, 0, sizeof(unsigned long long), stream);
+  e = cudaMemsetAsync(a.tile_ctr, 0, (kMixed ? 2 : 1) * sizeof(unsigned long long), stream);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, a, n_tiles);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, k8_map, v8_map, a, mx, n_tiles);
   return cudaGetLastError();
+}
+
+long long query_tiles(const PrefillArgs& a) {
+  const int tok_per_cta = kQTiles * (kRows / a.group);
+  const long long blocks = (a.max_q_len + tok_per_cta - 1) / tok_per_cta;
+  return blocks * a.B * a.Hkv;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& q_map,
+                                const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                cudaStream_t stream) {
+  const long long n_tiles = query_tiles(a);
+  if (n_tiles <= 0) return cudaSuccess;
+  // (the decode-item maps are not read by the plain kernel)
+  return launch_kernel<false>(a, MixedArgs{}, q_map, k_map, v_map, k_map, v_map, n_tiles, stream);
+}
+
+cudaError_t launch_mixed_bf16(const PrefillArgs& a, const MixedArgs& mx, const CUtensorMap& q_map,
+                              const CUtensorMap& k_map, const CUtensorMap& v_map,
+                              const CUtensorMap& k8_map, const CUtensorMap& v8_map,
+                              cudaStream_t stream) {
+  return launch_kernel<true>(a, mx, q_map, k_map, v_map, k8_map, v8_map, query_tiles(a), stream);
 }
 
 }  // namespace attn_sink

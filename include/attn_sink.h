@@ -124,6 +124,53 @@ ATTN_SINK_API size_t attn_sink_prefill_workspace_size(int32_t B, int32_t Hq, int
                                                       int32_t max_q_len);
 
 /*
+ * A mixed batch in one launch: decode rows and prefill (or verify) segments
+ * of one ragged batch over one page pool.  "Accelerating Sonar through
+ * speculation", section "Inferensi dengan Speculative Decoding", puts
+ * sequences at different stages into one batch; "GPT-OSS pada Hari ke-0",
+ * section "Atensi Sink", gives the attention they all compute.
+ *
+ * Sequences [0, num_decode) are decode rows: each holds exactly one query
+ * (cu_seqlens_q[b+1] - cu_seqlens_q[b] = 1; a sequence with more rows gets
+ * only its first row written), at position kv_len - 1, which sees every key.
+ * They run as split-KV decode work (chunks of 1024 keys x 8 KV heads, combined
+ * by the LSE merge, the sink in the first chunk only) on SMs of their own,
+ * while the other SMs run the query tiles of sequences [num_decode, B) as
+ * attn_sink_prefill does; one persistent launch claims both kinds of work
+ * from two device-side queues, plus the merge.  Results equal
+ * attn_sink_prefill over the whole batch (which would run each decode row as
+ * a query tile of its own) up to fp32 rounding.
+ *
+ *  Every argument but the ones below is that of attn_sink_prefill; max_q_len
+ *  bounds the q_len of sequences [num_decode, B).
+ *  num_decode   host, 0 <= num_decode <= B.
+ *  workspace    device scratch of at least attn_sink_mixed_workspace_size()
+ *               bytes, 256-byte aligned (bf16: required; fp32: unused).  It
+ *               holds the two claim counters (zeroed on the stream before the
+ *               kernel) and the decode rows' fp32 partial states; no contents
+ *               need to be preserved.  Calls that overlap on the GPU need
+ *               separate workspaces.
+ * Supported: bf16 with B <= 1024 and Hq <= 256 (else ATTN_SINK_ERR_UNSUPPORTED);
+ * fp32 runs the whole batch on the fp32 path.
+ */
+ATTN_SINK_API attn_sink_status attn_sink_mixed(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                 const int32_t* block_table, int32_t block_table_stride,
+                                 const float* sinks, void* out, float* lse, int32_t B,
+                                 int32_t num_decode, int32_t total_q, int32_t max_q_len,
+                                 int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                                 int32_t num_pages, float scale, int32_t causal,
+                                 attn_sink_dtype dtype, int32_t* err_flag, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_sink_mixed needs: the counters plus num_decode * Hq
+ * rows of partial states, as many per row as the table row (block_table_stride
+ * * page_size keys) holds 1024-key chunks.  Pure host function. */
+ATTN_SINK_API size_t attn_sink_mixed_workspace_size(int32_t num_decode, int32_t Hq, int32_t Hkv,
+                                                    int32_t D, int32_t block_table_stride,
+                                                    int32_t page_size);
+
+/*
  * Paged-KV decode, one query token per sequence, optionally split along the
  * key sequence ("GPT-OSS pada Hari ke-0", section "Atensi Sink": attention is
  * parallelised over heads and along the KV length, and the sink is counted in

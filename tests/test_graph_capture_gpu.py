@@ -107,3 +107,50 @@ def test_prefill_graph_replay_matches_eager(cuda_lib):
         ref, ref_lse, _ = oracle_problem(ref_batch).attention()
         compare(o_graph, l_graph, ref, ref_lse, what="prefill graph replay %d" % step)
     assert db.err.item() == 0
+
+
+def test_mixed_graph_replay_matches_eager(cuda_lib):
+    """attn_sink_mixed captured in a CUDA graph: its memset node restarts both claim
+    counters, so replays with new queries equal eager calls bitwise."""
+    gas = cuda_lib
+    rng = np.random.default_rng(43)
+    dec_kv = np.array([1500, 40, 3000], np.int64)
+    pre_q, pre_prefix = np.array([100, 33], np.int64), np.array([200, 0], np.int64)
+    kv = np.concatenate([dec_kv, pre_q + pre_prefix])
+    pool = W.make_pool(rng, kv, 8, 64, 16, W.BF16)
+    sinks = W.sinks_normal(rng, 64, 2.0)
+    q_lens = np.concatenate([np.ones(3, np.int64), pre_q])
+    q = W.make_queries(rng, int(q_lens.sum()), 64, 64, W.BF16)
+    batch = W.batch_from_pool(pool, np.arange(5), q_lens, q, sinks)
+    db = DeviceBatch(batch)
+    out = torch.empty_like(db.q)
+    lse = torch.empty(db.q.shape[:2], dtype=torch.float32, device="cuda")
+    wsb = torch.empty(gas.mixed_workspace_size(3, 64, 8, 64, batch.block_table.shape[1], 16),
+                      dtype=torch.uint8, device="cuda")
+
+    def call():
+        gas.mixed(db.q, db.k, db.v, db.cu, db.kv_lens, db.bt, db.sinks, num_decode=3, max_q_len=100,
+                  scale=batch.scale, out=out, lse=lse, workspace=wsb, err_flag=db.err)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for step in range(2):
+        q2 = W.make_queries(rng, int(q_lens.sum()), 64, 64, W.BF16)
+        db.q.copy_(torch.from_numpy(q2.view(np.int16)).view(torch.bfloat16).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        o_graph, l_graph = out.clone(), lse.clone()
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(o_graph, out) and torch.equal(l_graph, lse), "replay %d differs" % step
+        ref_batch = W.Batch(batch.dtype, q2, batch.k_cache, batch.v_cache, batch.cu_seqlens_q,
+                            batch.kv_lens, batch.block_table, batch.sinks, batch.scale)
+        ref, ref_lse, _ = oracle_problem(ref_batch).attention()
+        compare(o_graph, l_graph, ref, ref_lse, what="mixed graph replay %d" % step)
+    assert db.err.item() == 0
