@@ -19,11 +19,13 @@ import torch
 
 __all__ = ["load", "prefill", "mixed", "decode", "decode_append", "merge", "decode_workspace_size",
            "prefill_workspace_size", "mixed_workspace_size", "status_string",
-           "set_wait_limit_ns", "AttnSinkError", "LIB_PATH", "FLAG_BAD_PAGE", "FLAG_TIMEOUT"]
+           "set_wait_limit_ns", "AttnSinkError", "LIB_PATH", "FLAG_BAD_PAGE", "FLAG_TIMEOUT",
+           "SPLIT_PERSISTENT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn_sink.so")
 FLAG_BAD_PAGE, FLAG_TIMEOUT = 1, 2
+SPLIT_PERSISTENT = -1
 _BF16, _FP32 = 0, 1
 _LIB = None
 
@@ -130,6 +132,8 @@ def decode(q, k_cache, v_cache, kv_lens, block_table, sinks, *, scale=None, num_
            out=None, lse=None, workspace=None, err_flag=None, stream=None):
     """Paged decode with sinks.  q [B, Hq, D]; caches [pages, page_size, Hkv, D].
 
+    num_splits: 0 automatic chunks, 1 no split, S > 1 that many page-aligned
+    chunks, SPLIT_PERSISTENT (-1) persistent CTAs with equal shares of all keys.
     Returns (out [B, Hq, D] in q's dtype, lse [B, Hq] fp32).
     """
     lib = load()

@@ -86,8 +86,8 @@ extern "C" ATTN_SINK_API attn_sink_status attn_sink_decode_static_scratch(
                                  sinks, out, B, Hq, Hkv, D, page_size, num_pages, scale,
                                  num_splits, dtype);
   if (st != ATTN_SINK_OK || B == 0) return st;
-  // fp32 with num_splits == 0 runs unsplit and needs no scratch.
-  const int32_t splits = (dtype == ATTN_SINK_FP32 && num_splits == 0) ? 1 : num_splits;
+  // fp32 with num_splits <= 0 runs unsplit and needs no scratch.
+  const int32_t splits = (dtype == ATTN_SINK_FP32 && num_splits <= 0) ? 1 : num_splits;
   const size_t need =
       attn_sink_decode_workspace_size(B, Hq, Hkv, D, block_table_stride, page_size, splits);
   if (need > ATTN_SINK_STATIC_SCRATCH_BYTES) return ATTN_SINK_ERR_WORKSPACE;

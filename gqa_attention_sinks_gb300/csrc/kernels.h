@@ -58,6 +58,25 @@ struct DecodeArgs {
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const CUtensorMap& k_map,
                                const CUtensorMap& v_map, cudaStream_t stream);
 
+// Persistent ("stream-K") split decode: every CTA takes an equal, contiguous
+// share of all (sequence, group of kHeadsPerCta KV heads) key streams laid end
+// to end, split at the streams' boundaries into pieces.  A stream inside one
+// CTA's share is written directly; the pieces of a stream that spans CTAs
+// c_first..c_last go to partial slots 0..c_last-c_first of its rows for the
+// merge.  The shares come from prefix sums every CTA computes from kv_lens, so
+// no counter is needed (nothing to zero between calls).
+constexpr int kStreamMinShare = 32;      // 16-key units: shares are at least 512 keys
+constexpr int kStreamMaxStreams = 2048;  // B * ceil(Hkv / kHeadsPerCta) the prefix table holds
+struct StreamKArgs {
+  int n_groups;        // ceil(Hkv / kHeadsPerCta)
+  int* stream_start;   // workspace [B * n_groups + 1]: prefix sums of units (written by CTA 0)
+  int* shares;         // workspace [1]: the number of CTAs with a share (written by CTA 0)
+};
+
+cudaError_t launch_decode_streamk(const DecodeArgs& a, const StreamKArgs& sk,
+                                  const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                  unsigned grid, cudaStream_t stream);
+
 // ------------------------------------------------------------- KV append
 // Writes k_new / v_new [B, Hkv, 64] into the cache slot of position
 // kv_lens[b] - 1 of every sequence with kv_lens[b] >= 1 (any element size).
@@ -91,6 +110,13 @@ struct MergeArgs {
   // When set, row r = b * Hq + h writes output row seq_start[b] * Hq + h (the
   // decode rows of a ragged batch).
   const int32_t* seq_start;
+  // Stream-K decode (stream_start set): the parts of row r come from the CTAs
+  // whose shares its stream spans (see StreamKArgs); a stream without keys is
+  // written here (out = 0, lse = sink).
+  const int* stream_start;
+  const int* shares;
+  int group, n_groups;
+  const float* sinks;
 };
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);

@@ -30,7 +30,26 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(const MergeArgs a) {
   if (row >= a.rows) return;
 
   int n = a.num_parts;
-  if (a.kv_lens) {
+  if (a.stream_start) {
+    // Stream-K decode: the row's stream spans the shares c_first..c_last.
+    const int b = row / a.Hq, h = row % a.Hq;
+    const int s = b * a.n_groups + (h / a.group) / kHeadsPerCta;
+    const long long U = a.stream_start[(a.rows / a.Hq) * a.n_groups];
+    const long long G = *a.shares;
+    const long long x0 = a.stream_start[s], x1 = a.stream_start[s + 1];
+    if (x1 == x0) {  // no keys: only the sink (out = 0, lse = sink)
+      const long long base = static_cast<long long>(row) * kHeadDim + 2 * lane;
+      if (a.out_fp32)
+        *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + base) = make_float2(0.f, 0.f);
+      else
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + base) = 0u;
+      if (a.lse && lane == 0) a.lse[row] = a.sinks[h];
+      return;
+    }
+    const long long c_first = ((x0 + 1) * G - 1) / U, c_last = (x1 * G - 1) / U;
+    if (c_first == c_last) return;  // written directly by the decode kernel
+    n = static_cast<int>(min(c_last - c_first + 1, static_cast<long long>(a.s_stride)));
+  } else if (a.kv_lens) {
     int kv = max(0, a.kv_lens[row / a.Hq]);
     if (a.kv_cap > 0) kv = min(kv, a.kv_cap);
     const int units = (kv + kUnitTokens - 1) / kUnitTokens;

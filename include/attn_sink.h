@@ -73,6 +73,8 @@ typedef enum {
 } attn_sink_dtype;
 
 #define ATTN_SINK_FLAG_BAD_PAGE 1
+/* num_splits value of attn_sink_decode for the persistent split. */
+#define ATTN_SINK_SPLIT_PERSISTENT (-1)
 #define ATTN_SINK_FLAG_TIMEOUT 2
 
 /*
@@ -180,10 +182,19 @@ ATTN_SINK_API size_t attn_sink_mixed_workspace_size(int32_t num_decode, int32_t 
  *               position kv_len - 1 and sees every key 0..kv_len-1).
  *  kv_lens      device int32 [B] (0 allowed: out = 0, lse = sink).
  *  out          device [B, Hq, D] dtype; lse device fp32 [B, Hq] or NULL.
- *  num_splits   0: the library picks a chunk length in pages from B, Hkv and
- *               block_table_stride; 1: no split; S > 1: chunk c of S covers
- *               pages [floor(c*P/S), floor((c+1)*P/S)) with
- *               P = ceil(kv_len/page_size).  S <= 256.
+ *  num_splits   0: the library picks a chunk length in keys from B, Hkv,
+ *               block_table_stride and the SM count (one CTA per chunk, the
+ *               hardware hands the CTAs out); 1: no split; S > 1: chunk c of S
+ *               covers pages [floor(c*P/S), floor((c+1)*P/S)) with
+ *               P = ceil(kv_len/page_size), S <= 256;
+ *               ATTN_SINK_SPLIT_PERSISTENT (-1): persistent CTAs (three per
+ *               SM) each take an equal share of all sequences' keys laid end
+ *               to end, split at sequence boundaries; the shares come from
+ *               prefix sums of kv_lens computed on the device ("Accelerating
+ *               Sonar through speculation", section "Inferensi dengan
+ *               Speculative Decoding": the per-batch planning the pages do on
+ *               the CPU happens on the device).  Used when B * ceil(Hkv/4) <=
+ *               2048, otherwise the same as 0.  bf16 only (fp32: as 0).
  *  workspace    device scratch of at least attn_sink_decode_workspace_size()
  *               bytes, 256-byte aligned (may be NULL when that size is 0).
  *               Holds fp32 partial states between the split kernel and the

@@ -100,6 +100,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert _call_decode(lib, Hq=64, Hkv=2) == 2                # group 32 unsupported
     assert _call_decode(lib, q=256 + 4) == 1                   # misaligned q
     assert _call_decode(lib, S=300) == 1                       # too many splits
+    assert _call_decode(lib, S=-2) == 1                        # (-1 is the persistent split)
     assert _call_decode(lib, scale=float("nan")) == 1
     assert _call_decode(lib, S=4, ws=None, wsb=0) == 3         # missing workspace
     assert _call_decode(lib, S=4, ws=256 + 16, wsb=1 << 20) == 3   # misaligned workspace

@@ -41,7 +41,7 @@ def _hidden_last(seed, lens, Hq=64, Hkv=8):
     return full, hidden, k_new, v_new
 
 
-@pytest.mark.parametrize("Hkv,num_splits", [(8, 0), (8, 7), (2, 0), (6, 3)])
+@pytest.mark.parametrize("Hkv,num_splits", [(8, 0), (8, 7), (2, 0), (6, 3), (8, -1), (6, -1)])
 def test_decode_append_bf16(cuda_lib, Hkv, num_splits):
     lens = [1, 16, 17, 300, 1000, 2049, 64, 5]
     full, hidden, k_new, v_new = _hidden_last(50 + Hkv, lens, Hq=8 * Hkv, Hkv=Hkv)

@@ -24,7 +24,7 @@ def _small_decode(seed=5, num_seqs=7, kv=(1, 700), Hq=64, Hkv=8, sink_std=2.0, k
     return W.batch_from_pool(pool, np.arange(len(lens)), np.ones(len(lens), np.int64), q, sinks)
 
 
-@pytest.mark.parametrize("num_splits", [0, 1, 2, 7, 32])
+@pytest.mark.parametrize("num_splits", [0, 1, 2, 7, 32, -1])
 def test_decode_parity_small(cuda_lib, num_splits):
     batch = _small_decode()
     db = DeviceBatch(batch)
@@ -38,7 +38,7 @@ def test_decode_parity_small(cuda_lib, num_splits):
 def test_decode_group_sizes(cuda_lib, group, Hkv):
     batch = _small_decode(seed=6, num_seqs=3, kv=(5, 300), Hq=group * Hkv, Hkv=Hkv)
     db = DeviceBatch(batch)
-    for S in (0, 3):
+    for S in (0, 3, -1):
         out, lse = _decode(cuda_lib, db, S)
         ref, ref_lse, _ = oracle_problem(batch).attention()
         compare(out, lse, ref, ref_lse, what="group %d S=%d" % (group, S))
@@ -51,7 +51,7 @@ def test_decode_single_kv_head(cuda_lib, Hq):
     batch = _small_decode(seed=12, num_seqs=5, kv=(1, 900), Hq=Hq, Hkv=1)
     db = DeviceBatch(batch)
     ref, ref_lse, _ = oracle_problem(batch).attention()
-    for S in (0, 3):
+    for S in (0, 3, -1):
         out, lse = _decode(cuda_lib, db, S)
         compare(out, lse, ref, ref_lse, what="MQA decode Hq %d S=%d" % (Hq, S))
     assert db.err.item() == 0
@@ -64,7 +64,7 @@ def test_decode_edge_lengths(cuda_lib):
     batch.sinks[:4] = -math.inf                       # sink -inf with kv_len 0 -> lse -inf
     db = DeviceBatch(batch)
     ref, ref_lse, _ = oracle_problem(batch).attention()
-    for S in (0, 1, 4, 40):
+    for S in (0, 1, 4, 40, -1):
         out, lse = _decode(cuda_lib, db, S)
         compare(out, lse, ref, ref_lse, what="edge S=%d" % S)
         assert db.err.item() == 0
@@ -106,7 +106,7 @@ def test_decode_page_table_bitwise(cuda_lib):
                     np.where(batch.block_table >= 0, inv[np.maximum(batch.block_table, 0)], -1).astype(np.int32),
                     batch.sinks, batch.scale)
     a, b = DeviceBatch(batch), DeviceBatch(moved)
-    for S in (0, 3):
+    for S in (0, 3, -1):
         oa, la = _decode(cuda_lib, a, S)
         ob, lb = _decode(cuda_lib, b, S)
         assert bool((oa == ob).all()) and bool((la == lb).all())
@@ -119,7 +119,7 @@ def test_decode_bad_page_sets_flag(cuda_lib):
     db = DeviceBatch(batch)
     ref, ref_lse, bad = oracle_problem(batch).attention()
     assert bad > 0
-    for S in (0, 1, 5):
+    for S in (0, 1, 5, -1):
         db.err.zero_()
         out, lse = _decode(cuda_lib, db, S)
         assert db.err.item() & cuda_lib.FLAG_BAD_PAGE
@@ -182,6 +182,8 @@ def test_decode_gptoss_full(cuda_lib):
     out, lse = _decode(cuda_lib, db, 0)
     ref, ref_lse, _ = oracle_problem(batch).attention()
     compare(out, lse, ref, ref_lse, what="gpt-oss decode")
+    out_p, lse_p = _decode(cuda_lib, db, -1)         # the persistent split
+    compare(out_p, lse_p, ref, ref_lse, what="gpt-oss decode, persistent split")
     assert db.err.item() == 0
 
 

@@ -19,21 +19,25 @@ def _decode_batch(seed, lens):
     return W.batch_from_pool(pool, np.arange(len(lens)), np.ones(len(lens), np.int64), q, sinks)
 
 
-def test_decode_graph_replay_matches_eager(cuda_lib):
+@pytest.mark.parametrize("num_splits", [0, -1])
+def test_decode_graph_replay_matches_eager(cuda_lib, num_splits):
+    """Decode captured once and replayed while the KV lengths change: the split
+    plan (automatic chunks, or the persistent split's shares) is derived on the
+    device at every replay."""
     gas = cuda_lib
     lens0 = np.array([700, 33, 512, 900, 1, 257], np.int64)
     batch = _decode_batch(40, lens0)
     db = DeviceBatch(batch)
     B, Hq, D = db.q.shape
     Hkv, ps = db.k.shape[2], db.k.shape[1]
-    ws = torch.empty(max(256, gas.decode_workspace_size(B, Hq, Hkv, D, db.bt.shape[1], ps, 0)),
+    ws = torch.empty(max(256, gas.decode_workspace_size(B, Hq, Hkv, D, db.bt.shape[1], ps, num_splits)),
                      dtype=torch.uint8, device="cuda")
     out = torch.empty_like(db.q)
     lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
 
     def call():
         gas.decode(db.q, db.k, db.v, db.kv_lens, db.bt, db.sinks, scale=batch.scale, out=out,
-                   lse=lse, workspace=ws, err_flag=db.err)
+                   lse=lse, workspace=ws, num_splits=num_splits, err_flag=db.err)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())

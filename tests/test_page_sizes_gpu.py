@@ -35,7 +35,7 @@ def test_prefill_page_sizes(cuda_lib, page_size):
     assert db.err.item() == 0
 
 
-@pytest.mark.parametrize("page_size,num_splits", [(32, 0), (64, 0), (64, 3), (256, 0), (256, 2)])
+@pytest.mark.parametrize("page_size,num_splits", [(32, 0), (64, 0), (64, 3), (256, 0), (256, 2), (64, -1)])
 def test_decode_page_sizes(cuda_lib, page_size, num_splits):
     batch = _batch(70 + page_size, [1] * 6, [0, 15, 200, 1023, 3000, 512], page_size, decode=True)
     db = DeviceBatch(batch)
