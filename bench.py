@@ -48,10 +48,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
-                                               "kernels.h")],
-                "sha256": "", "bytes": None},
-    "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu")],
-               "sha256": "", "bytes": None},
+                                               "kernels.h", "decode_unit.cuh")],
+                "sha256": "852b5a3e0a024270b668e9443947e3f9ac879b74e588bd29145e47a0fe62f7ba", "bytes": 690049024},
+    "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu",
+                                              "decode_unit.cuh")],
+               "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 582872832},
 }
 
 
