@@ -49,7 +49,7 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "kernels.h", "decode_unit.cuh")],
-                "sha256": "852b5a3e0a024270b668e9443947e3f9ac879b74e588bd29145e47a0fe62f7ba", "bytes": 690049024},
+                "sha256": "b919c42dc8b1127c824e186aa97626a142906bf53430ad1674017b3cd5e7b32e", "bytes": 557989376},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu",
                                               "decode_unit.cuh")],
                "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 582872832},
