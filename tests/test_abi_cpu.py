@@ -170,3 +170,44 @@ def test_static_scratch_checks_arguments_like_decode(lib):
     assert call(S=300) == 1 and call(D=128) == 2
     assert call() == 3                    # valid, but its partials exceed the static array
     assert call(B=0) == 0
+
+
+def _call_mixed(lib, **kw):
+    # Fake, 256-aligned addresses: every call below is rejected by the host
+    # checks before anything touches them.
+    args = dict(q=256, k=512, v=768, cu=1024, kv=1280, bt=1536, stride=4, sinks=1792, out=2048,
+                lse=None, B=4, nd=2, total_q=8, max_q=4, Hq=8, Hkv=2, D=64, ps=16, pages=8,
+                scale=0.125, causal=1, dt=0, err=None, ws=4096, wsb=1 << 20, stream=None)
+    args.update(kw)
+    f = lib.attn_sink_mixed
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    f.argtypes = [vp] * 6 + [i32, vp, vp, vp] + [i32] * 9 + [ctypes.c_float, i32, i32, vp, vp,
+                                                              ctypes.c_size_t, vp]
+    f.restype = i32
+    a = args
+    return f(a["q"], a["k"], a["v"], a["cu"], a["kv"], a["bt"], a["stride"], a["sinks"], a["out"],
+             a["lse"], a["B"], a["nd"], a["total_q"], a["max_q"], a["Hq"], a["Hkv"], a["D"],
+             a["ps"], a["pages"], a["scale"], a["causal"], a["dt"], a["err"], a["ws"], a["wsb"],
+             a["stream"])
+
+
+def test_mixed_host_validation_and_workspace_size(lib):
+    size = lib.attn_sink_mixed_workspace_size
+    size.argtypes = [ctypes.c_int32] * 6
+    size.restype = ctypes.c_size_t
+    # counters, plus num_decode * Hq rows of partials when a row can span several
+    # 1024-key items (8192-key table rows: 8 slots)
+    rows, slots = 48 * 64, 8
+    parts = -(-rows * slots * 64 * 4 // 256) * 256 + -(-rows * slots * 4 // 256) * 256
+    assert size(48, 64, 8, 64, 512, 16) == 256 + parts
+    assert size(48, 64, 8, 64, 64, 16) == 256          # one item per row: no partials
+    assert size(48, 64, 8, 128, 512, 16) == 0          # unsupported head dim
+    assert _call_mixed(lib, nd=5) == 1                 # num_decode > B
+    assert _call_mixed(lib, nd=-1) == 1
+    assert _call_mixed(lib, q=None) == 1
+    assert _call_mixed(lib, D=128) == 2
+    assert _call_mixed(lib, B=1025, nd=0) == 2         # bf16: the sequences must fit shared memory
+    assert _call_mixed(lib, Hq=512, Hkv=32) == 2
+    assert _call_mixed(lib, ws=None, wsb=0) == 3       # bf16 needs the workspace
+    assert _call_mixed(lib, ws=4096 + 64) == 3         # misaligned
+    assert _call_mixed(lib, B=0, nd=0) == 0            # empty batch is a no-op

@@ -111,3 +111,16 @@ def test_mixed_gptoss_full(cuda_lib):
     512-token chunks over prefixes up to 16k, 1% outlier keys: every row."""
     batch = W.mixed_batch()["single"]
     _check(cuda_lib, batch, batch.meta["n_decode"], "mixed batch, one launch, every row")
+
+
+def test_mixed_fp32(cuda_lib):
+    """fp32 inputs run the whole mixed batch on the fp32 path (decode rows included)."""
+    rng = np.random.default_rng(69)
+    dec_kv, pre_q, pre_prefix = np.array([40, 90]), np.array([16, 5]), np.array([48, 0])
+    kv = np.concatenate([dec_kv, pre_q + pre_prefix])
+    pool = W.make_pool(rng, kv, 2, 64, 16, W.FP32)
+    sinks = W.sinks_normal(rng, 8, 1.0)
+    q_lens = np.concatenate([np.ones(2, np.int64), pre_q])
+    q = W.make_queries(rng, int(q_lens.sum()), 8, 64, W.FP32)
+    batch = W.batch_from_pool(pool, np.arange(4), q_lens, q, sinks, True, W.FP32)
+    _check(cuda_lib, batch, 2, "mixed fp32")
