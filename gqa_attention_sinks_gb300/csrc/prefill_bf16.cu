@@ -112,6 +112,13 @@ constexpr int kTileRing = 4;
 // softmax warps.
 constexpr int kTileReaders = 1 + kQTiles + kSoftmaxWarps;
 
+// A work tile: its sequence b, KV head g, query rows and the key tiles they
+// see, derived from its linear index.
+struct WorkTile {
+  int b, g, q_start, q_len, tok0, kv_raw, kv_len, n_kv;
+  int first_pos;  // absolute position of the tile's first query (fits: kv_len, q_len < 2^31)
+};
+
 struct alignas(8) Bars {
   uint64_t q_full[kQBufs];
   uint64_t q_empty[kQBufs];   // both Q tiles' MMAs of the buffer's work tile are done
@@ -127,6 +134,7 @@ struct alignas(8) Bars {
   uint64_t tile_full[kTileRing];   // the slot holds the next claimed tile
   uint64_t tile_empty[kTileRing];  // every reader has taken the slot's tile
   long long tile_slot[kTileRing];  // claimed tile index, or -1: no tile left
+  WorkTile tile_w[kTileRing];      // a claimed query tile, decoded once by the claiming warp
   uint32_t unit_ok[kStages];  // bit u: 16-key unit u of the stage's tile was loaded
   uint32_t s_uok[kQTiles];    // unit_ok of the stage the current S was computed from
   uint32_t tmem_base;
@@ -140,12 +148,6 @@ struct Meta {
   const int32_t* cu_seqlens_q;
   const int32_t* kv_lens;
   const float* sinks;
-};
-
-// A work tile, derived identically by every role from its linear index.
-struct WorkTile {
-  int b, g, q_start, q_len, tok0, kv_raw, kv_len, n_kv;
-  int first_pos;  // absolute position of the tile's first query (fits: kv_len, q_len < 2^31)
 };
 
 // Query block r of sequence b (r = 0 is the last block): its first query
@@ -480,16 +482,18 @@ __device__ __forceinline__ long long claim_work(const PrefillArgs& a, const Mixe
   return -1;
 }
 
-// A reader role takes claimed tile number i from the ring (warp-collective).
-// Returns false when the pipeline aborted; t = -1 means no tile is left.
+// A reader role takes claimed tile number i from the ring (warp-collective),
+// and, if w is given, its decoded work tile when it is a query tile.  Returns
+// false when the pipeline aborted; t = -1 means no tile is left.
 template <bool kPoll>
-__device__ __forceinline__ bool take_tile(Bars* bars, int i, long long& t, volatile int* abort_word,
-                                          const PrefillArgs& a) {
+__device__ __forceinline__ bool take_tile(Bars* bars, int i, long long& t, WorkTile* w,
+                                          volatile int* abort_word, const PrefillArgs& a) {
   const int slot = i % kTileRing;
   const bool ready = mbar_wait<kPoll>(&bars->tile_full[slot], (i / kTileRing) & 1, abort_word,
                                       a.err_flag, a.wait_limit_ns);
   if (!__all_sync(0xffffffffu, ready)) return false;
   t = *reinterpret_cast<volatile long long*>(&bars->tile_slot[slot]);
+  if (w && t >= 0) *w = bars->tile_w[slot];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&bars->tile_empty[slot]);
   return true;
@@ -618,12 +622,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     Claimer claimer;
     for (int i = 0; ok; ++i) {
       long long t;
+      WorkTile w;
       if (is_k) {
         // Claim the next tile and publish it to the other roles.
         if constexpr (kMixed)
           t = claim_work<kMixed>(a, mx, meta, n_tiles, tok_per_cta, sort_keys, n_sorted, info, claimer);
         else
           t = claim_tile(a, meta, n_tiles, tok_per_cta, sort_keys, n_sorted);
+        if (!kMixed && t >= 0)  // a claimed tile always holds query rows
+          decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
         const int slot = i % kTileRing;
         if (i >= kTileRing) {
           const bool ready = mbar_wait<kPoll>(&bars->tile_empty[slot], ((i / kTileRing) + 1) & 1,
@@ -632,12 +639,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         if (lane == 0) {
+          if (!kMixed && t >= 0) bars->tile_w[slot] = w;  // (the mixed kernel's readers decode it)
           bars->tile_slot[slot] = t;
           mbar_arrive(&bars->tile_full[slot]);  // release: the slot is written
         }
         __syncwarp();
       } else {
-        ok = take_tile<kPoll>(bars, i, t, abort_word, a);
+        ok = take_tile<kPoll>(bars, i, t, kMixed ? nullptr : &w, abort_word, a);
         if (!ok) break;
       }
       if constexpr (kMixed) {
@@ -690,8 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         if (t < 0) break;
       }
-      WorkTile w;
-      decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);  // a claimed tile always holds query rows
+      // (The mixed kernel's readers decode the tile themselves: with the
+      // decode items' code beside it, the copy measured slower.)
+      if constexpr (kMixed) decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
       if (is_k && w.kv_len < w.kv_raw && lane == 0 && a.err_flag) atomicOr(a.err_flag, kFlagBadPage);
       if (w.n_kv == 0) continue;
       if (is_k) {
@@ -808,7 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int i = 0; ok; ++i) {
       long long t;
-      ok = take_tile<kPoll>(bars, i, t, abort_word, a);
+      WorkTile w;
+      ok = take_tile<kPoll>(bars, i, t, kMixed ? nullptr : &w, abort_word, a);
       if constexpr (kMixed) {
         if (!ok || t == -1) break;
         if (is_decode_item(t)) {  // its stages go to the softmax warps
@@ -820,8 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         if (!ok || t < 0) break;
       }
-      WorkTile w;
-      decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
+      if constexpr (kMixed) decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
       if (w.n_kv == 0) continue;
       const int qb = qw % kQBufs;
       // Q loaded, the first K/V tile in, and the previous S read out of TMEM.
@@ -884,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int i = 0; ok; ++i) {
       long long t;
-      ok = take_tile<kPoll>(bars, i, t, abort_word, a);
+      ok = take_tile<kPoll>(bars, i, t, nullptr, abort_word, a);
       if constexpr (kMixed) {
       if (!ok || t == -1) break;
       if (is_decode_item(t)) {
@@ -946,6 +955,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         if (!ok || t < 0) break;
       }
+      // This warp decodes the tile itself: copying the published one measured
+      // slower here (more register spills in the softmax loop).
       WorkTile w;
       decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
       const int tok = w.tok0 + q * tok_per_tile + r / a.group;
