@@ -217,14 +217,6 @@ struct SchedInfo {
   unsigned long long dec_units;   // decode units (16 keys x Hkv heads each)
 };
 
-// Builds the sorted list in shared memory (all threads of the CTA).  Every
-// CTA builds the same list: the keys are distinct, so their sorted order does
-// not depend on where each thread placed them.  Returns the number of query
-// blocks; kAllAlike when every sequence has the same query and key lengths
-// (claims then walk groups of (sequence, KV head) pairs, longest blocks first
-// within each group, so a group's K/V stays in L2 while its tiles run, and the
-// last claims are short tiles); -1 when the list is not used (more than
-// kSortMax blocks, or the metadata is not in shared memory).
 // Pads keys[n..) to a power of two and sorts them ascending (bitonic; all
 // threads of the CTA).
 __device__ __forceinline__ void sort_keys_ascending(uint32_t* keys, int n) {
@@ -250,6 +242,14 @@ __device__ __forceinline__ void sort_keys_ascending(uint32_t* keys, int n) {
   }
 }
 
+// Builds the sorted list in shared memory (all threads of the CTA).  Every
+// CTA builds the same list: the keys are distinct, so their sorted order does
+// not depend on where each thread placed them.  Returns the number of query
+// blocks; kAllAlike when every sequence has the same query and key lengths
+// (claims then walk groups of (sequence, KV head) pairs, longest blocks first
+// within each group, so a group's K/V stays in L2 while its tiles run, and the
+// last claims are short tiles); -1 when the list is not used (more than
+// kSortMax blocks, or the metadata is not in shared memory).
 __device__ __forceinline__ int build_sorted_blocks(const PrefillArgs& a, const Meta& m, bool meta_in_smem,
                                    int tok_per_cta, uint32_t* keys, int* counter) {
   if (!meta_in_smem || a.B > 1024) return -1;
@@ -274,26 +274,7 @@ __device__ __forceinline__ int build_sorted_blocks(const PrefillArgs& a, const M
   __syncthreads();
   const int n = *counter;
   if (n > kSortMax) return -1;
-  int pow2 = 1;
-  while (pow2 < n) pow2 <<= 1;
-  for (int i = n + threadIdx.x; i < pow2; i += blockDim.x) keys[i] = 0xFFFFFFFFu;
-  __syncthreads();
-  // bitonic sort, ascending
-  for (int k = 2; k <= pow2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
-        const int l = i ^ j;
-        if (l > i) {
-          const uint32_t x = keys[i], y = keys[l];
-          if (((i & k) == 0) == (x > y)) {
-            keys[i] = y;
-            keys[l] = x;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
+  sort_keys_ascending(keys, n);
   return n;
 }
 
