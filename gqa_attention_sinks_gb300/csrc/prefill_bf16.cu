@@ -872,9 +872,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // decode items' units in the mixed kernel).
     int it = 0, kv_it = 0;
     bool ok = true;
+    // The plain kernel takes the next work tile (decoded by the claiming warp)
+    // before writing the current one's output: the take then overlaps the wait
+    // for the last P*V instead of following the output stores.
+    long long t_next = 0;
+    WorkTile w_next;
+    bool have_next = false;
+    // This thread's row of a Q tile: its token offset and its query head in the
+    // group (the plain kernel keeps them across tiles).
+    const int row_tok = q * tok_per_tile + r / a.group, row_head = r % a.group;
     for (int i = 0; ok; ++i) {
       long long t;
-      ok = take_tile<kPoll>(bars, i, t, nullptr, abort_word, a);
+      if (!kMixed && have_next)
+        t = t_next;
+      else
+        ok = take_tile<kPoll>(bars, i, t, nullptr, abort_word, a);
       if constexpr (kMixed) {
       if (!ok || t == -1) break;
       if (is_decode_item(t)) {
@@ -936,12 +948,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         if (!ok || t < 0) break;
       }
-      // This warp decodes the tile itself: copying the published one measured
-      // slower here (more register spills in the softmax loop).
+      // The first tile (and every tile of the mixed kernel) is decoded here.
       WorkTile w;
-      decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
-      const int tok = w.tok0 + q * tok_per_tile + r / a.group;
-      const int head = w.g * a.group + r % a.group;
+      if (!kMixed && have_next)
+        w = w_next;
+      else
+        decode_tile<kMixed>(a, meta, t, tok_per_cta, w, mx.num_decode);
+      have_next = false;
+      const int tok = w.tok0 + (kMixed ? q * tok_per_tile + r / a.group : row_tok);
+      const int head = w.g * a.group + (kMixed ? r % a.group : row_head);
       const bool row_valid = tok < w.q_len;
       const int pos = w.kv_len - w.q_len + tok;  // fits: kv_len, q_len < 2^31
       float m_run = meta.sinks[head] * kLog2e;  // the sink is the initial running max ...
@@ -1113,6 +1128,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars->p_ready[q]);
       }
       if (!ok) break;
+      if constexpr (!kMixed) {
+        ok = take_tile<kPoll>(bars, i + 1, t_next, &w_next, abort_word, a);
+        if (!ok) break;
+        have_next = true;
+      }
 
       // -------------------------------------------------------------- epilogue
       uint32_t o[2][32];
