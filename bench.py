@@ -49,7 +49,7 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "kernels.h", "decode_unit.cuh")],
-                "sha256": "b3808e5c407b49a1f17032d190a1b9edbc0bf065414a45c45c836d4b340c14fa", "bytes": 557653504},
+                "sha256": "e67aaaa64d4af848658902d92b732463752ef82d2e67e9ee2602467656b18e10", "bytes": 557655808},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu",
                                               "decode_unit.cuh")],
                "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 582872832},
