@@ -874,7 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     // The plain kernel takes the next work tile (decoded by the claiming warp)
     // before writing the current one's output: the take then overlaps the wait
-    // for the last P*V instead of following the output stores.
+    // for the last P*V instead of following the output stores.  (The mixed
+    // kernel, whose ring also carries decode items, measured 0.4 % slower with
+    // the same early take.)
     long long t_next = 0;
     WorkTile w_next;
     bool have_next = false;
