@@ -49,7 +49,7 @@ CSRC = "gqa_attention_sinks_gb300/csrc/"
 NCU_TRAFFIC = {
     "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
                                                "kernels.h", "decode_unit.cuh")],
-                "sha256": "e67aaaa64d4af848658902d92b732463752ef82d2e67e9ee2602467656b18e10", "bytes": 557655808},
+                "sha256": "bb828355fd0bdc36391d33dd78bfa3481aebf76a05f0e0f827d1f0a5305f5df9", "bytes": 557818624},
     "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu",
                                               "decode_unit.cuh")],
                "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 582872832},
