@@ -46,13 +46,23 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # value holds only for the kernel sources it was captured with (sha256 over the
 # listed files); after any change to them the roofline reports traffic = null.
 CSRC = "gqa_attention_sinks_gb300/csrc/"
+PREFILL_SOURCES = [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh", "kernels.h",
+                                      "decode_unit.cuh")]
+DECODE_SOURCES = [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu",
+                                     "decode_unit.cuh")]
 NCU_TRAFFIC = {
-    "prefill": {"files": [CSRC + f for f in ("prefill_bf16.cu", "tcgen05.cuh", "ptx.cuh",
-                                               "kernels.h", "decode_unit.cuh")],
+    # prefill_kernel, 8 x 4096 causal prefill
+    "prefill": {"files": PREFILL_SOURCES,
                 "sha256": "bb828355fd0bdc36391d33dd78bfa3481aebf76a05f0e0f827d1f0a5305f5df9", "bytes": 557818624},
-    "decode": {"files": [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu",
-                                              "decode_unit.cuh")],
+    # decode_split_kernel, gpt-oss decode (64 seqs)
+    "decode": {"files": DECODE_SOURCES,
                "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 582872832},
+    # decode_split_kernel, long split decode (4 x 131072 keys, 32 chunks)
+    "long": {"files": DECODE_SOURCES, "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 1074084864},
+    # decode_split_kernel, the mixed batch's decode part
+    "mixed_decode": {"files": DECODE_SOURCES, "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 1647429376},
+    # prefill_kernel, the mixed batch's chunked-prefill part
+    "mixed_prefill": {"files": PREFILL_SOURCES, "sha256": "bb828355fd0bdc36391d33dd78bfa3481aebf76a05f0e0f827d1f0a5305f5df9", "bytes": 69377024},
 }
 
 
@@ -547,7 +557,7 @@ def run_ours(args, ws, rank, local):
     if args.workload in ("all", "long"):
         batch = W.long_split_decode(seed=20260004 + so)
         name = "long split-KV decode: 4 seqs x 131072 keys, 32 chunks, Hq 64, Hkv 8, D 64, bf16"
-        part, _, d = arm.decode_part(batch, 32, name, max(3, min(steps, 100)), None)
+        part, _, d = arm.decode_part(batch, 32, name, max(3, min(steps, 100)), "long")
         if want_cpu:
             part["cpu_baseline"] = cpu_oracle_rate(batch, args.cpu_seconds, "GB/s")
         arm.release(d)
@@ -559,10 +569,10 @@ def run_ours(args, ws, rank, local):
         k = max(3, min(steps, 100))
         dpart, dstep, d = arm.decode_part(
             m["decode"], 0, "mixed batch, decode part: 48 seqs, KV U[1024, 32768], Hq 64, Hkv 8, "
-            "D 64, bf16, 1% outlier keys", k, None)
+            "D 64, bf16, 1% outlier keys", k, "mixed_decode")
         ppart, pstep = arm.prefill_part(
             m["prefill"], "mixed batch, chunked-prefill part: 4 x 512 new tokens over prefixes "
-            "U[0, 16384], Hq 64, Hkv 8, D 64, bf16, 1% outlier keys", k, None)
+            "U[0, 16384], Hq 64, Hkv 8, D 64, bf16, 1% outlier keys", k, "mixed_prefill")
 
         def both():
             dstep()
