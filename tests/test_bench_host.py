@@ -91,3 +91,18 @@ def test_timed_region_max_over_two_gloo_ranks():
     assert n0 == n1 == 5
     assert ms0 == ms1                                  # the same maximum on both ranks
     assert 3 * 40 <= ms0 < 3 * 40 + 200                # rank 1's three 40 ms steps
+
+
+def test_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
+    """A pinned ncu traffic figure holds for the kernel sources it was captured
+    with: a different source hash makes the roofline report no traffic."""
+    for kind, e in bench.NCU_TRAFFIC.items():
+        assert e["files"] and all(f.startswith(bench.CSRC) for f in e["files"]), kind
+        got = bench.ncu_traffic(kind)
+        if e["sha256"] == bench.sources_sha256(e["files"]) and e["bytes"]:
+            assert got == e["bytes"]
+        else:
+            assert got is None
+    monkeypatch.setattr(bench, "sources_sha256", lambda files: "0" * 64)
+    assert all(bench.ncu_traffic(k) is None for k in bench.NCU_TRAFFIC)
+    assert bench.ncu_traffic("no such workload") is None
