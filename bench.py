@@ -53,7 +53,7 @@ DECODE_SOURCES = [CSRC + f for f in ("decode_bf16.cu", "ptx.cuh", "kernels.h", "
 NCU_TRAFFIC = {
     # prefill_kernel, 8 x 4096 causal prefill
     "prefill": {"files": PREFILL_SOURCES,
-                "sha256": "bb828355fd0bdc36391d33dd78bfa3481aebf76a05f0e0f827d1f0a5305f5df9", "bytes": 557818624},
+                "sha256": "dc6ed89ce508011f2a9b1d313a3cd31b0af19e29b2627eed5da828007bf18104", "bytes": 557558272},
     # decode_split_kernel, gpt-oss decode (64 seqs)
     "decode": {"files": DECODE_SOURCES,
                "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 582872832},
@@ -62,7 +62,7 @@ NCU_TRAFFIC = {
     # decode_split_kernel, the mixed batch's decode part
     "mixed_decode": {"files": DECODE_SOURCES, "sha256": "d5359e965e705dc861d4b523f8eb32a6d2cb78e9cb8da3267774bc3ca019f032", "bytes": 1647429376},
     # prefill_kernel, the mixed batch's chunked-prefill part
-    "mixed_prefill": {"files": PREFILL_SOURCES, "sha256": "bb828355fd0bdc36391d33dd78bfa3481aebf76a05f0e0f827d1f0a5305f5df9", "bytes": 69377024},
+    "mixed_prefill": {"files": PREFILL_SOURCES, "sha256": "dc6ed89ce508011f2a9b1d313a3cd31b0af19e29b2627eed5da828007bf18104", "bytes": 69377024},
 }
 
 

@@ -13,9 +13,10 @@
 // list ordered longest rows first (the last query block of every sequence,
 // then the one before, ...).  CTAs claim tiles from that list at run time
 // through a counter in the caller's workspace, so a CTA that drew short tiles
-// takes more of them (greedy longest-first assignment); the Q/K producer warp
-// claims, and hands each claimed tile to the other roles through a small ring
-// in shared memory.
+// takes more of them (greedy longest-first assignment).  The Q/K producer warp
+// claims each tile, decodes it once and hands it to the other roles through a
+// small ring in shared memory; the softmax warps take the next tile from the
+// ring before writing the current tile's output.
 //
 // Warp roles (384 threads):
 //   warps 0-3  softmax for Q tile 0, warps 4-7 softmax for Q tile 1: one
